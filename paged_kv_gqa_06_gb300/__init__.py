@@ -1,0 +1,32 @@
+"""Paged-KV decode attention for GB300 (sm_103a).
+
+Two operations, implemented as hand-written CUDA kernels behind a C ABI
+(``include/forge_paged.h``, ``libforge_paged.so``):
+
+  * ``forge_paged_kv_append`` -- scatter each sequence's new K/V token into
+    its slot of the paged block pool;
+  * ``forge_paged_gqa_decode`` -- grouped-query attention of one new query
+    token per sequence over that sequence's cached K/V, read through its
+    block table, with split-K partials merged by a reduce kernel.
+
+The Python functions of the same names (``paged_kv_gqa_06_gb300.binding``)
+only marshal torch tensors into the C descriptors.  The CUDA library is
+loaded on first use; if it is missing the call raises -- there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+__all__ = [
+    "forge_paged_kv_append",
+    "forge_paged_gqa_decode",
+    "forge_paged_gqa_decode_ex",
+    "forge_paged_gqa_decode_workspace_bytes",
+    "forge_paged_get_device_error",
+]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

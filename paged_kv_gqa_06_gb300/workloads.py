@@ -1,0 +1,252 @@
+"""Seeded synthetic inputs for paged-KV append + paged GQA decode.
+
+This module is the one thing the CUDA path and the CPU oracle share: it makes
+the inputs (numpy arrays of bf16 bit patterns and int32/int64 index arrays)
+and holds none of the method's arithmetic -- no dot products, no softmax, no
+address translation of cache rows.  It plays the host-side block allocator of
+a serving engine (forge-engine README, "What it implements": a paged block
+allocator owns the KV pool) so that each sequence owns a list of physical
+blocks and the new token of this step has a slot.
+
+Shapes follow the attention layers of the two model sizes the pages name
+(Qwen3-4B in the forge-engine README, Qwen3-0.6B in "Make the Engine Talk"),
+plus a tiny case, a skewed long-context case and a 36-layer batch step.
+
+Recipe (every config):
+  * context_lens: the lengths AFTER this step's append; the appended token
+    sits at position L-1.
+  * Blocks: BS = 16 tokens.  The pool holds NB blocks.  Physical ids are a
+    seeded random permutation of range(NB), handed out to sequences in order;
+    ids the permutation leaves over are free blocks scattered through the
+    pool.  Unused block-table entries are -1.
+  * Values: float32 N(0, 1) draws from numpy's PCG64, rounded to bf16 with
+    round-to-nearest-even.  Config "qwen3_4b" doubles K (an exact power-of-two
+    scale) so that logits reach about +-8.
+  * Poison: every cache slot that holds no token before the append -- free
+    blocks, the tail of each sequence's last block, and the append target
+    itself -- is bf16 NaN (0x7FC0), so a kernel that reads a slot it should
+    not read, or skips the append, produces NaN.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+BLOCK_SIZE = 16
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Inputs are finite normal draws here, so NaN/Inf handling is not needed.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(rng: np.random.Generator, shape, mul: float = 1.0) -> np.ndarray:
+    """bf16 bits of mul * N(0,1) (mul a power of two, so the scaling is exact)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    chunk = 1 << 22
+    buf = np.empty(min(n, chunk), dtype=np.float32)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        view = buf[: e - s]
+        rng.standard_normal(out=view, dtype=np.float32)
+        if mul != 1.0:
+            view *= np.float32(mul)
+        out[s:e] = f32_to_bf16_bits(view)
+    return out.reshape(shape)
+
+
+@dataclasses.dataclass
+class Spec:
+    """Shape recipe for one named workload."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    out_dtype: str            # "f32" or "bf16"
+    lens: str                 # "fixed", "uniform", "lognormal"
+    fixed_lens: tuple = ()
+    lo: int = 1
+    hi: int = 1
+    median: float = 1.0
+    sigma: float = 1.0
+    k_mul: float = 1.0
+    free_frac: float = 0.0    # fraction of the pool left free (interleaved)
+    nb_fixed: int = 0         # pool size when fixed by the recipe
+    layers: int = 1
+    seed: int = 0
+    description: str = ""
+
+
+SPECS = {
+    "tiny": Spec(
+        "tiny", B=4, Hq=8, Hkv=2, D=64, out_dtype="f32", lens="fixed",
+        fixed_lens=(7, 16, 33, 64), nb_fixed=32, seed=1001,
+        description="batch 4, lens {7,16,33,64}, 8/2 heads, D 64, 32-block pool, fp32 out"),
+    "qwen3_0_6b": Spec(
+        "qwen3_0_6b", B=8, Hq=16, Hkv=8, D=128, out_dtype="bf16", lens="uniform",
+        lo=128, hi=2048, seed=1002,
+        description="Qwen3-0.6B-shaped layer: batch 8, lens U[128,2048], 16/8 heads, D 128, bf16 out"),
+    "qwen3_4b": Spec(
+        "qwen3_4b", B=32, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="uniform",
+        lo=512, hi=8192, k_mul=2.0, free_frac=0.10, seed=1003,
+        description="Qwen3-4B-shaped layer: batch 32, lens U[512,8192], 32/8 heads, D 128, "
+                    "10% free blocks interleaved, K x2, bf16 out"),
+    "skewed": Spec(
+        "skewed", B=4, Hq=32, Hkv=8, D=128, out_dtype="f32", lens="fixed",
+        fixed_lens=(32768, 1024, 256, 17), seed=1004,
+        description="skewed long context: lens {32768,1024,256,17}, 32/8 heads, D 128, fp32 out"),
+    "skewed_bf16": Spec(
+        "skewed_bf16", B=4, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="fixed",
+        fixed_lens=(32768, 1024, 256, 17), seed=1004,
+        description="skewed long context, bf16 out"),
+    "cb36": Spec(
+        "cb36", B=64, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="lognormal",
+        lo=1, hi=16384, median=1024.0, sigma=1.0, layers=36, seed=1005,
+        description="continuous-batching step over 36 layers: batch 64, lens lognormal "
+                    "(median 1024, sigma 1) clipped to [1,16384], 32/8 heads, D 128, bf16"),
+}
+
+
+@dataclasses.dataclass
+class Workload:
+    """One batch of decode inputs.  Arrays are numpy; bf16 tensors are uint16 bits.
+
+    Per-layer tensors come from ``layer(l)`` so that a many-layer step can be
+    produced (and checked) one layer at a time.
+    """
+    spec: Spec
+    seed: int
+    NB: int
+    MB: int
+    context_lens: np.ndarray   # int32 [B]
+    block_tables: np.ndarray   # int32 [B, MB]
+    slot_mapping: np.ndarray   # int64 [B]
+    scale: float               # float32 value, passed to both sides
+
+    @property
+    def B(self): return self.spec.B
+
+    @property
+    def Hq(self): return self.spec.Hq
+
+    @property
+    def Hkv(self): return self.spec.Hkv
+
+    @property
+    def D(self): return self.spec.D
+
+    @property
+    def BS(self): return BLOCK_SIZE
+
+    @property
+    def layers(self): return self.spec.layers
+
+    def layer(self, l: int = 0) -> dict:
+        """q, k_new, v_new and the pre-append (poisoned) caches of layer ``l``."""
+        s = self.spec
+        rng = np.random.default_rng([self.seed, 1 + l])
+        q = _normal_bf16(rng, (s.B, s.Hq, s.D))
+        k_new = _normal_bf16(rng, (s.B, s.Hkv, s.D), s.k_mul)
+        v_new = _normal_bf16(rng, (s.B, s.Hkv, s.D))
+        shape = (self.NB, s.Hkv, BLOCK_SIZE, s.D)
+        k_cache = _normal_bf16(rng, shape, s.k_mul)
+        v_cache = _normal_bf16(rng, shape)
+        pb, po = np.nonzero(self.poison_mask())
+        k_cache[pb, :, po, :] = BF16_NAN
+        v_cache[pb, :, po, :] = BF16_NAN
+        return dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache)
+
+    def poison_mask(self) -> np.ndarray:
+        """bool [NB, BS]: slots holding no token before this step's append."""
+        holds = np.zeros((self.NB, BLOCK_SIZE), dtype=bool)
+        for b in range(self.B):
+            n_before = int(self.context_lens[b]) - 1   # tokens already cached
+            for j in range(-(-n_before // BLOCK_SIZE) if n_before > 0 else 0):
+                p = int(self.block_tables[b, j])
+                cnt = min(BLOCK_SIZE, n_before - j * BLOCK_SIZE)
+                holds[p, :cnt] = True
+        return ~holds
+
+    def bytes_decode(self, out_bytes: int | None = None) -> int:
+        """Algorithmic bytes of one decode call: q + K/V rows of every cached
+        token + the output.  (Accounting, not arithmetic of the method.)"""
+        s = self.spec
+        ob = out_bytes if out_bytes is not None else (4 if s.out_dtype == "f32" else 2)
+        tok = int(self.context_lens.astype(np.int64).sum())
+        return s.B * s.Hq * s.D * 2 + tok * s.Hkv * s.D * 2 * 2 + s.B * s.Hq * s.D * ob
+
+    def bytes_append(self) -> int:
+        """Bytes one append call moves: new K/V rows read and written."""
+        rows = int((self.slot_mapping >= 0).sum())
+        return rows * self.Hkv * self.D * 2 * 2 * 2
+
+
+def _lengths(spec: Spec, rng: np.random.Generator) -> np.ndarray:
+    if spec.lens == "fixed":
+        return np.array(spec.fixed_lens, dtype=np.int32)
+    if spec.lens == "uniform":
+        return rng.integers(spec.lo, spec.hi, size=spec.B, endpoint=True).astype(np.int32)
+    if spec.lens == "lognormal":
+        x = np.exp(rng.normal(math.log(spec.median), spec.sigma, size=spec.B))
+        return np.clip(np.rint(x), spec.lo, spec.hi).astype(np.int32)
+    raise ValueError(spec.lens)
+
+
+def make_workload(name_or_spec, seed: int | None = None, context_lens=None) -> Workload:
+    """Build the index structures of a named (or custom) workload.
+
+    ``context_lens`` overrides the recipe's lengths (edge-case tests).
+    """
+    spec = SPECS[name_or_spec] if isinstance(name_or_spec, str) else name_or_spec
+    seed = spec.seed if seed is None else int(seed)
+    rng = np.random.default_rng([seed, 0])
+    lens = _lengths(spec, rng) if context_lens is None else np.asarray(context_lens, np.int32)
+    if lens.shape != (spec.B,):
+        raise ValueError("context_lens must have one entry per sequence")
+    nblk = [-(-int(L) // BLOCK_SIZE) for L in lens]
+    needed = sum(nblk)
+    if spec.nb_fixed:
+        NB = spec.nb_fixed
+        if NB < needed:
+            raise ValueError("pool too small for these lengths")
+    elif spec.free_frac > 0:
+        NB = math.ceil(needed / (1.0 - spec.free_frac))
+    else:
+        NB = needed
+    MB = max(1, max(nblk) if nblk else 1)
+    perm = rng.permutation(NB).astype(np.int32)
+    tables = np.full((spec.B, MB), -1, dtype=np.int32)
+    slots = np.full(spec.B, -1, dtype=np.int64)
+    pos = 0
+    for b, n in enumerate(nblk):
+        tables[b, :n] = perm[pos:pos + n]
+        pos += n
+        L = int(lens[b])
+        if L > 0:
+            t = L - 1                     # the appended token's position
+            slots[b] = int(tables[b, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE
+    scale = float(np.float32(1.0 / math.sqrt(spec.D)))
+    return Workload(spec=spec, seed=seed, NB=NB, MB=MB, context_lens=lens.astype(np.int32),
+                    block_tables=tables, slot_mapping=slots, scale=scale)
+
+
+def custom_spec(name="custom", **kw) -> Spec:
+    """A Spec for tests: any field of ``Spec`` may be given."""
+    base = dict(B=2, Hq=8, Hkv=2, D=64, out_dtype="f32", lens="fixed", fixed_lens=(1, 1), seed=7)
+    base.update(kw)
+    return Spec(name, **base)
