@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark: one decode step of the paged-KV hot path on GB300.
+
+A step is the whole hot path over one batch: forge_paged_kv_append (scatter
+this step's new K/V token of every sequence into its cache slot) followed by
+forge_paged_gqa_decode (split kernel + split reduce).  The default workload
+is the Qwen3-4B-shaped attention layer: batch 32, context lengths uniform in
+[512, 8192], 32 query / 8 KV heads, head_dim 128, 16-token blocks, 10 % free
+blocks interleaved in the pool, bf16 storage.
+
+Reported metric: decode KV-read bandwidth in GB/s (algorithmic bytes = q +
+every cached token's K and V rows + out, per step) and microseconds per
+layer-step.  Inputs are larger than L2 (the KV pool is ~0.63 GB against a
+126 MB L2), so no flush is done between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU ("replicas only": the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-GQA decode: KV-read HBM GB/s (% of GB300 peak) and µs per layer-step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+def _traffic_from_profile(src_hash: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_split_qwen3_4b.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != src_hash:
+        return None
+    try:
+        return int(vals["dram_bytes_per_decode_call"])
+    except (KeyError, ValueError):
+        return None
+
+
+def _decode_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh", "abi.cu"):
+        with open(os.path.join(ROOT, "paged_kv_gqa_06_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", gpu_id,
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + r[0].strip().split(".")[1]) if "." in r[0] else 0.0
+                rows.append(dict(t=ts, sm=float(r[1]), max=float(r[2]), power=r[3].strip(),
+                                 hw=r[4].strip(), hwt=r[5].strip(), swt=r[6].strip(), pcap=r[7].strip()))
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        inside = [r for r in rows if t0 - 0.15 <= r["t"] <= t1 + 0.15]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in use:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in use),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "whole run (timed region shorter than one sample)"}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+def _seq_bytes(wl, b, out_bytes):
+    return wl.Hq * wl.D * 2 + int(wl.context_lens[b]) * wl.Hkv * wl.D * 4 + wl.Hq * wl.D * out_bytes
+
+
+def _config_dict(wl, extra=None):
+    s = wl.spec
+    lens = wl.context_lens
+    d = {"workload": f"{s.name}: {s.description}", "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv,
+         "head_dim": s.D, "block_size": 16, "pool_blocks": wl.NB, "tokens": int(lens.sum()),
+         "context_len_min": int(lens.min()), "context_len_max": int(lens.max()), "seed": wl.seed,
+         "out_dtype": s.out_dtype, "parallelism": "replicas (one independent batch per GPU)"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+
+def _oracle_prepare(wl):
+    import oracle
+    t = wl.layer(0)
+    kc, vc = t["k_cache"].copy(), t["v_cache"].copy()
+    oracle.paged_kv_append(t["k_new"], t["v_new"], wl.slot_mapping, kc, vc)
+    return t, kc, vc
+
+
+def _oracle_step(wl, t, kc, vc, seqs, threads):
+    """Append + decode for a subset of sequences with the CPU oracle."""
+    import oracle
+    sel = np.asarray(seqs)
+    oracle.paged_kv_append(t["k_new"][sel], t["v_new"][sel], wl.slot_mapping[sel], kc, vc)
+    oracle.paged_gqa_decode(t["q"][sel], kc, vc, wl.block_tables[sel], wl.context_lens[sel], wl.scale,
+                            nthreads=threads)
+
+
+def cpu_baseline(wl, out_bytes, budget_s=12.0):
+    """The oracle as it stands on this host's cores, over whole passes of the
+    workload until about budget_s of work (at least one pass)."""
+    import oracle
+    threads = oracle.host_cores()
+    t, kc, vc = _oracle_prepare(wl)
+    all_seqs = list(range(wl.B))
+    per_pass = sum(_seq_bytes(wl, b, out_bytes) for b in all_seqs)
+    passes, elapsed = 0, 0.0
+    t0 = time.perf_counter()
+    while passes < 1 or (elapsed < budget_s and passes < 20):
+        _oracle_step(wl, t, kc, vc, all_seqs, threads)
+        passes += 1
+        elapsed = time.perf_counter() - t0
+    gbs = per_pass * passes / elapsed / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{passes} full pass(es) of the workload (append + decode of all {wl.B} sequences), "
+                      f"{elapsed:.1f} s, fp64 C oracle with {threads} threads",
+            "ms_per_step": round(1e3 * elapsed / passes, 3)}
+
+
+def run_reference(args, wl, out_bytes):
+    """--impl reference: the CPU oracle as the reference arm."""
+    import oracle
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    threads = oracle.host_cores()
+    t, kc, vc = _oracle_prepare(wl)
+    # size each step's sample (a rotating subset of sequences) so that the
+    # whole run takes about two minutes of CPU time
+    probe0 = time.perf_counter()
+    _oracle_step(wl, t, kc, vc, [0], threads)
+    per_seq = max(1e-4, time.perf_counter() - probe0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nseq = int(max(1, min(wl.B, budget / per_seq)))
+    order = list(range(wl.B))
+    cursor = 0
+
+    def next_sample():
+        nonlocal cursor
+        s = [order[(cursor + i) % wl.B] for i in range(nseq)]
+        cursor = (cursor + nseq) % wl.B
+        return s
+
+    for _ in range(args.warmup):
+        _oracle_step(wl, t, kc, vc, next_sample(), threads)
+    total_bytes = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s = next_sample()
+        _oracle_step(wl, t, kc, vc, s, threads)
+        total_bytes += sum(_seq_bytes(wl, b, out_bytes) for b in s)
+    el = time.perf_counter() - t0
+    gbs = total_bytes / el / 1e9
+    sample = (f"each step: append + decode of {nseq} of the {wl.B} sequences (rotating), "
+              f"fp64 C oracle, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config_dict(wl),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+# --------------------------------------------------------------------------- GPU leg
+
+def run_native(args, wl, out_bytes):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_gqa_06_gb300 import binding
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+
+    t = wl.layer(0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = {"q": bf(t["q"]).pin_memory(), "k_new": bf(t["k_new"]).pin_memory(),
+            "v_new": bf(t["v_new"]).pin_memory(), "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+            "tables": torch.from_numpy(wl.block_tables).pin_memory(),
+            "lens": torch.from_numpy(wl.context_lens).pin_memory()}
+    d = {k: v.to(dev) for k, v in host.items()}
+    k_cache = bf(t["k_cache"]).to(dev)
+    v_cache = bf(t["v_cache"]).to(dev)
+    del t
+    out_dt = torch.bfloat16 if wl.spec.out_dtype == "bf16" else torch.float32
+    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=out_dt, device=dev)
+    host_out = torch.empty(out.shape, dtype=out_dt).pin_memory()
+
+    stream = torch.cuda.Stream(device=dev)
+    bytes_step = wl.bytes_decode(out_bytes)
+    launches_per_step = 1 + 1 + (1 if wl.MB * 16 > 512 else 0)
+
+    def step(ev_a=None, ev_b=None):
+        binding.forge_paged_kv_append(d["k_new"], d["v_new"], d["slots"], k_cache, v_cache, stream=stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale, out,
+                                       stream=stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    def e2e_step():
+        for k in ("q", "k_new", "v_new", "slots", "tables", "lens"):
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    assert binding.forge_paged_get_device_error(stream) == 0
+
+    # ---------------- timed region (device-resident inputs)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(_gpu_id(torch, dev.index or 0)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(args.steps):
+            step(ev_a[k], ev_b[k])
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    if ws > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    decode_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    rows = sampler.stop() if sampler else []
+    clocks = ClockSampler.summarize(rows, w0, w1) if sampler else None
+
+    # ---------------- end to end: host buffers, copies inside the timed region
+    e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    if ws > 1:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e2e_start.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e2e_start.elapsed_time(e2e_end)
+    assert binding.forge_paged_get_device_error(stream) == 0
+    assert torch.isfinite(host_out.float()).all()
+
+    if ws > 1:
+        tt = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total, e2e_ms = float(tt[0]), float(tt[1])
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return None
+
+    peak, peak_src = _peaks()
+    ms_step = ms_total / args.steps
+    value = ws * bytes_step * args.steps / (ms_total * 1e-3) / 1e9
+    dec_avg_ms = statistics.fmean(decode_ms)
+    achieved = bytes_step / (dec_avg_ms * 1e-3) / 1e9
+    traffic = _traffic_from_profile(_decode_source_hash())
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k_new", "v_new", "slots", "tables", "lens"))
+    d2h = host_out.numel() * host_out.element_size()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_layer_step": round(ms_step * 1e3, 2),
+        "pct_of_hbm_peak": round(100.0 * value / ws / peak, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "config": _config_dict(wl, {"l2": "no flush: inputs larger than L2 (KV pool "
+                                          f"{2 * k_cache.numel() * 2 / 1e6:.0f} MB vs 126 MB L2)",
+                                    "bytes_per_step": bytes_step,
+                                    "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
+        "roofline": {"bound": "hbm", "kernel": "forge_paged_gqa_decode (split kernel + split reduce)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "decode_us": round(dec_avg_ms * 1e3, 2),
+                     "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src},
+        "e2e": {"value": round(ws * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if ws > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="qwen3_4b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from paged_kv_gqa_06_gb300 import workloads as W
+    wl = W.make_workload(args.workload)
+    if wl.layers != 1:
+        raise SystemExit("bench.py times single-layer workloads; the 36-layer step is a parity test")
+    out_bytes = 4 if wl.spec.out_dtype == "f32" else 2
+
+    if args.impl == "reference":
+        line = run_reference(args, wl, out_bytes)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    ws, _, local = _dist()
+    if local == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    else:  # another rank on this node builds; wait for its library
+        from paged_kv_gqa_06_gb300 import binding
+        for _ in range(600):
+            if os.path.exists(binding.LIB_PATH):
+                break
+            time.sleep(0.5)
+    line = run_native(args, wl, out_bytes)
+    if line is None:
+        return 0
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, out_bytes)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * forge_paged.h -- C ABI of libforge_paged.so: paged-KV append and paged
+ * grouped-query-attention decode on NVIDIA GB300 (sm_103a).
+ *
+ * What the operations are (page title, section):
+ *   - forge-engine README, "What it implements", row "KV cache": the KV cache
+ *     is a pool of fixed-size blocks handed out by a block allocator; row
+ *     "Kernels": decode attention over that cache is a CUDA paged GQA kernel.
+ *   - "Make the Engine Talk", 1.2 "The loop behind it": after the prefill,
+ *     every decode pass runs the model on ONE new token per sequence and the
+ *     cache grows by that token; 1.3 "What the rest of Part I builds": the
+ *     attention is grouped-query attention.
+ *
+ * Definitions (the plain reading where the pages give no formula):
+ *   BS = 16 tokens per block.  Token t of sequence b lives in physical block
+ *   block_tables[b][t / BS], slot t % BS.  With G = Hq / Hkv, query head h
+ *   reads KV head h / G (contiguous groups).  For every b, h:
+ *     out[b,h,:] = sum_{t < L_b} softmax_t(scale * q[b,h,:] . K_b[t,:]) V_b[t,:]
+ *   with L_b = context_lens[b] (the length AFTER this step's append); out is
+ *   zero when L_b == 0.  Cache slots at t >= L_b, free blocks and unused
+ *   block-table entries are never read, whatever they hold.
+ *
+ * Tensors are passed as forge_tensor descriptors (below).  All data pointers
+ * are device pointers on the current CUDA device.  The caller owns every
+ * tensor; the library keeps no pointer after a call returns.
+ *
+ * Every call is asynchronous: it validates its arguments on the host,
+ * enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) and returns.  No call reads device memory from the host, so calls
+ * can be captured in a CUDA graph (see forge_paged_gqa_decode for its
+ * workspace note).  Calls never abort, throw or trap: they return a
+ * forge_status.  Argument errors are reported before anything is enqueued.
+ * Violations of the device-side preconditions (a block id outside the pool,
+ * a length longer than the table row, a slot outside the pool) make the
+ * kernels skip the bad access and record an error code that
+ * forge_paged_get_device_error returns.
+ */
+#ifndef FORGE_PAGED_H
+#define FORGE_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FORGE_API __attribute__((visibility("default")))
+#else
+#define FORGE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FORGE_BF16 = 1, /* bfloat16 */
+    FORGE_F32 = 2,  /* float32 */
+    FORGE_I32 = 3,  /* int32 */
+    FORGE_I64 = 4   /* int64 */
+} forge_dtype;
+
+/* A strided view of device memory.  shape/stride beyond ndim are ignored.
+ * Strides are in ELEMENTS, not bytes. */
+typedef struct {
+    void *data;
+    int32_t dtype; /* forge_dtype */
+    int32_t ndim;  /* 1..4 */
+    int64_t shape[4];
+    int64_t stride[4];
+} forge_tensor;
+
+typedef enum {
+    FORGE_OK = 0,
+    FORGE_ERR_NULL = -1,        /* a descriptor or a needed data pointer is NULL */
+    FORGE_ERR_DTYPE = -2,       /* wrong dtype */
+    FORGE_ERR_SHAPE = -3,       /* wrong rank, mismatched sizes or unsupported strides */
+    FORGE_ERR_UNSUPPORTED = -4, /* valid but not built: D, block size or group size */
+    FORGE_ERR_ALIGN = -5,       /* a data pointer or stride breaks 16-byte alignment */
+    FORGE_ERR_CUDA = -6,        /* a CUDA runtime call or a launch failed */
+    FORGE_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than required */
+    FORGE_ERR_VALUE = -8        /* a scalar argument is out of range (e.g. non-finite scale) */
+} forge_status;
+
+/* Device-side error codes (forge_paged_get_device_error). */
+#define FORGE_DEVERR_NONE 0
+#define FORGE_DEVERR_BLOCK_ID 1   /* a used block-table entry is outside [0, NB) */
+#define FORGE_DEVERR_LENGTH 2     /* context_lens[b] > MB * BS (or negative) */
+#define FORGE_DEVERR_SLOT 3       /* slot_mapping[b] >= NB * BS */
+#define FORGE_DEVERR_TIMEOUT 4    /* a pipeline wait gave up (should never happen) */
+
+/*
+ * forge_paged_kv_append -- write this step's new K/V token of every sequence
+ * into its cache slot ("Make the Engine Talk", 1.2: each decode pass adds the
+ * new token to the cache).
+ *
+ *   k_new, v_new   bf16 [B, Hkv, D]; innermost stride 1, other strides
+ *                  multiples of 8 elements; data 16-byte aligned.
+ *   slot_mapping   int64 [B], contiguous.  slot = block * BS + offset.
+ *                  A negative slot skips that row (padding).  Two rows with
+ *                  the same non-negative slot are a precondition violation
+ *                  (which row wins is undefined).  slot >= NB*BS is skipped
+ *                  and flagged FORGE_DEVERR_SLOT.
+ *   k_cache,
+ *   v_cache        bf16 [NB, Hkv, BS, D], modified in place.  BS must be 16.
+ *                  stride[3] == 1 and stride[2] == D (each (block, head)
+ *                  tile is one contiguous BS*D run); stride[0], stride[1]
+ *                  multiples of 8 elements; data 16-byte aligned.
+ *   stream         cudaStream_t to enqueue on.
+ *
+ * Supported: D a multiple of 8 (any D the decode supports).  The copy is
+ * bit-exact.  Nothing but the addressed slots changes.
+ */
+FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tensor *v_new,
+                          const forge_tensor *slot_mapping, forge_tensor *k_cache,
+                          forge_tensor *v_cache, void *stream);
+
+/*
+ * forge_paged_gqa_decode -- grouped-query attention of one query token per
+ * sequence over that sequence's paged K/V (forge-engine README, "What it
+ * implements", row "Kernels": CUDA paged GQA; definition at the top of this
+ * file).
+ *
+ *   q              bf16 [B, Hq, D]; innermost stride 1; data 16-B aligned;
+ *                  strides multiples of 8 elements.
+ *   k_cache,
+ *   v_cache        bf16 [NB, Hkv, BS, D] with the layout rules of append.
+ *   block_tables   int32 [B, MB]; stride[1] == 1.  Entries past a
+ *                  sequence's last block are never read (any value).
+ *   context_lens   int32 [B], contiguous.  0 <= L_b <= MB * BS.
+ *   scale          logit scale (finite), e.g. 1/sqrt(D).
+ *   out            [B, Hq, D] bf16 (rounded to nearest even) or f32;
+ *                  innermost stride 1; strides multiples of 8 elements.
+ *   stream         cudaStream_t.
+ *
+ * Supported: D in {64, 128}; BS = 16; G = Hq/Hkv in {1, 2, 4, 8}.
+ * Work is split along the context in splits of up to 512 tokens (fewer for
+ * short tables); sequences with more than one split are merged by a second
+ * kernel.  The split scratch is a per-(device, stream) buffer that the
+ * library allocates with cudaMalloc on first need and keeps, growing it when
+ * a larger problem arrives; the first call of a given size on a stream
+ * should therefore come before any stream capture.  Use
+ * forge_paged_gqa_decode_ex to pass caller-owned scratch instead.
+ * Thread-safe.
+ */
+FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *k_cache,
+                           const forge_tensor *v_cache, const forge_tensor *block_tables,
+                           const forge_tensor *context_lens, float scale, forge_tensor *out,
+                           void *stream);
+
+/*
+ * Bytes of split scratch that forge_paged_gqa_decode_ex needs for these
+ * sizes and split length.  split_tokens = 0 picks the same split length as
+ * forge_paged_gqa_decode; otherwise it must be a multiple of 16 in
+ * [16, 1024].  Returns 0 for invalid sizes.  Host-only, no CUDA call.
+ */
+FORGE_API size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                              int max_blocks_per_seq, int split_tokens);
+
+/*
+ * forge_paged_gqa_decode_ex -- forge_paged_gqa_decode with caller-owned
+ * scratch (device memory, 256-byte aligned, at least
+ * forge_paged_gqa_decode_workspace_bytes(...) bytes; may be NULL only when
+ * that size is 0) and an explicit split length in tokens (0 = automatic,
+ * else a multiple of 16 in [16, 1024]).  Allocates nothing.  Calls that
+ * share one workspace must not overlap on the GPU.
+ */
+FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tensor *k_cache,
+                              const forge_tensor *v_cache, const forge_tensor *block_tables,
+                              const forge_tensor *context_lens, float scale, forge_tensor *out,
+                              void *workspace, size_t workspace_bytes, int split_tokens,
+                              void *stream);
+
+/* Human-readable name of a forge_status.  Never NULL. */
+FORGE_API const char *forge_status_string(int status);
+
+/*
+ * Read and clear the device-side error code (FORGE_DEVERR_*) of the current
+ * device.  Synchronises `stream` first, so it reports errors of work enqueued
+ * before it.  Returns FORGE_OK or FORGE_ERR_CUDA / FORGE_ERR_NULL.
+ */
+FORGE_API int forge_paged_get_device_error(void *stream, int *code_out);
+
+/* Library version, e.g. "0.1.0". */
+FORGE_API const char *forge_paged_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORGE_PAGED_H */

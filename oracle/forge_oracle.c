@@ -128,11 +128,11 @@ static int decode_one(const decode_job *j, int b, int h, double *K, double *V,
         s[t] = exp(s[t] - m);
         den += s[t];
     }
-    for (int d = 0; d < D; ++d) {
-        double num = 0.0;
-        for (int t = 0; t < L; ++t) num += s[t] * V[(size_t)t * D + d];
-        o[d] = num / den;
-    }
+    /* numerators: for every d the sum runs over t in ascending order */
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int t = 0; t < L; ++t)
+        for (int d = 0; d < D; ++d) o[d] += s[t] * V[(size_t)t * D + d];
+    for (int d = 0; d < D; ++d) o[d] /= den;
     return ORACLE_OK;
 }
 

@@ -1,0 +1,156 @@
+"""ctypes binding of libforge_paged.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls, takes torch CUDA
+tensors, builds the ``forge_tensor`` descriptors (data pointer, dtype,
+shape, element strides), passes the current torch CUDA stream unless one is
+given, and turns a negative status into an exception.  No arithmetic of the
+operations happens here, and there is no fallback: if the library is not
+built the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libforge_paged.so")
+
+FORGE_BF16, FORGE_F32, FORGE_I32, FORGE_I64 = 1, 2, 3, 4
+_DTYPES = {torch.bfloat16: FORGE_BF16, torch.float32: FORGE_F32,
+           torch.int32: FORGE_I32, torch.int64: FORGE_I64}
+
+FORGE_OK = 0
+STATUS_NAMES = {0: "FORGE_OK", -1: "FORGE_ERR_NULL", -2: "FORGE_ERR_DTYPE", -3: "FORGE_ERR_SHAPE",
+                -4: "FORGE_ERR_UNSUPPORTED", -5: "FORGE_ERR_ALIGN", -6: "FORGE_ERR_CUDA",
+                -7: "FORGE_ERR_WORKSPACE", -8: "FORGE_ERR_VALUE"}
+DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "context length longer than the table row",
+                 3: "slot outside the pool", 4: "pipeline wait timed out"}
+
+
+class ForgeTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class ForgeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) and type the C entry points.  Raises if the library is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+                "(the CUDA library is required: there is no CPU path)")
+        lib = ctypes.CDLL(path)
+        T = ctypes.POINTER(ForgeTensor)
+        P = ctypes.c_void_p
+        lib.forge_paged_kv_append.argtypes = [T, T, T, T, T, P]
+        lib.forge_paged_kv_append.restype = ctypes.c_int
+        lib.forge_paged_gqa_decode.argtypes = [T, T, T, T, T, ctypes.c_float, T, P]
+        lib.forge_paged_gqa_decode.restype = ctypes.c_int
+        lib.forge_paged_gqa_decode_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, P, ctypes.c_size_t,
+                                                  ctypes.c_int, P]
+        lib.forge_paged_gqa_decode_ex.restype = ctypes.c_int
+        lib.forge_paged_gqa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
+        lib.forge_paged_gqa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.forge_status_string.argtypes = [ctypes.c_int]
+        lib.forge_status_string.restype = ctypes.c_char_p
+        lib.forge_paged_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        lib.forge_paged_get_device_error.restype = ctypes.c_int
+        lib.forge_paged_version.argtypes = []
+        lib.forge_paged_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def describe(t: torch.Tensor | None) -> ForgeTensor | None:
+    """forge_tensor descriptor of a torch tensor (no copy)."""
+    if t is None:
+        return None
+    if t.dim() > 4:
+        raise ValueError("forge tensors have at most 4 dims")
+    d = ForgeTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else 0
+    d.dtype = _DTYPES.get(t.dtype, 0)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _raise(status: int, what: str):
+    if status != FORGE_OK:
+        msg = load_library().forge_status_string(status).decode()
+        raise ForgeError(status, f"{what}: {msg}")
+
+
+def forge_paged_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Scatter the new K/V token of every row into its slot (in place)."""
+    lib = load_library()
+    rc = lib.forge_paged_kv_append(_ref(describe(k_new)), _ref(describe(v_new)), _ref(describe(slot_mapping)),
+                                   _ref(describe(k_cache)), _ref(describe(v_cache)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_kv_append")
+
+
+def forge_paged_gqa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):
+    """Paged GQA decode into ``out`` (bf16 or fp32 [B, Hq, D]); returns ``out``."""
+    lib = load_library()
+    rc = lib.forge_paged_gqa_decode(_ref(describe(q)), _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                    _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                    float(scale), _ref(describe(out)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_gqa_decode")
+    return out
+
+
+def forge_paged_gqa_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks_per_seq, split_tokens=0) -> int:
+    return int(load_library().forge_paged_gqa_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks_per_seq,
+                                                                      split_tokens))
+
+
+def forge_paged_gqa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                              workspace=None, split_tokens=0, stream=None):
+    """Decode with caller-owned scratch (a uint8 CUDA tensor) and an explicit split length."""
+    lib = load_library()
+    ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.forge_paged_gqa_decode_ex(_ref(describe(q)), _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                       _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                       float(scale), _ref(describe(out)), ws_ptr, ws_bytes,
+                                       int(split_tokens), _stream_ptr(stream))
+    _raise(rc, "forge_paged_gqa_decode_ex")
+    return out
+
+
+def forge_paged_get_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error code."""
+    code = ctypes.c_int(0)
+    rc = load_library().forge_paged_get_device_error(_stream_ptr(stream), ctypes.byref(code))
+    _raise(rc, "forge_paged_get_device_error")
+    return code.value

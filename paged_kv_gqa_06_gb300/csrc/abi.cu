@@ -1,0 +1,390 @@
+// C ABI of libforge_paged.so (declared in include/forge_paged.h).
+//
+// Host side only: argument validation, split planning from host-known shapes
+// (no device reads, so calls stay asynchronous and capturable), the split
+// workspace cache, the device error word, and the kernel launches.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/forge_paged.h"
+#include "common.cuh"
+
+namespace {
+
+using forge::kBlockSize;
+
+// Device error word: the first device-side precondition violation since the
+// last forge_paged_get_device_error call.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultSplitTokens = 512;
+constexpr int kMaxSplitTokens = 1024;  // producer lanes hold <= 64 table entries
+constexpr int kMinSplitTokens = 16;
+
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+// Split workspace owned by the library, per (device, stream).
+std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return FORGE_ERR_CUDA;
+  return FORGE_OK;
+}
+
+// Address of this device's error word (looked up once per device) and its SM count.
+int device_state(int dev, int** err, int* sms) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return FORGE_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FORGE_ERR_CUDA;
+    g_num_sms[dev] = n;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *err = g_err_ptr[dev];
+  *sms = g_num_sms[dev];
+  return FORGE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_tensor(const forge_tensor* t, int dtype, int ndim) {
+  if (!t) return FORGE_ERR_NULL;
+  if (t->dtype != dtype) return FORGE_ERR_DTYPE;
+  if (t->ndim != ndim) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return FORGE_ERR_SHAPE;
+  return FORGE_OK;
+}
+
+int64_t numel(const forge_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// bf16 tensor read/written in 16-byte vectors along its last dim: innermost
+// stride 1, other strides multiples of 8 elements, data 16-byte aligned.
+int check_vec16(const forge_tensor* t, int elem_bytes) {
+  if (numel(t) == 0) return FORGE_OK;
+  if (!t->data) return FORGE_ERR_NULL;
+  if (t->stride[t->ndim - 1] != 1) return FORGE_ERR_SHAPE;
+  const int64_t per16 = 16 / elem_bytes;
+  for (int i = 0; i < t->ndim - 1; ++i)
+    if (t->stride[i] % per16 != 0) return FORGE_ERR_ALIGN;
+  if (!aligned16(t->data)) return FORGE_ERR_ALIGN;
+  return FORGE_OK;
+}
+
+// [NB, Hkv, BS, D] bf16 cache: each (block, head) tile contiguous.
+int check_cache(const forge_tensor* c) {
+  int rc = check_tensor(c, FORGE_BF16, 4);
+  if (rc) return rc;
+  if (c->shape[2] != kBlockSize) return FORGE_ERR_UNSUPPORTED;
+  if (numel(c) == 0) return FORGE_OK;
+  if (c->stride[3] != 1 || c->stride[2] != c->shape[3]) return FORGE_ERR_SHAPE;
+  return check_vec16(c, 2);
+}
+
+#define FORGE_TRY(expr)      \
+  do {                       \
+    int _rc = (expr);        \
+    if (_rc != FORGE_OK) return _rc; \
+  } while (0)
+
+struct DecodePlan {
+  forge::DecodeParams p;
+  int D, G;
+  bool out_bf16;
+  size_t ws_bytes;
+};
+
+int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms) {
+  if (split_tokens > 0) return split_tokens / kBlockSize;
+  // Automatic: 512-token splits, shortened while the upper bound on CTAs
+  // (every sequence as long as its table row) would not fill ~4 CTAs per SM
+  // twice over.
+  int bps = kDefaultSplitTokens / kBlockSize;
+  const int64_t want = 8ll * (num_sms > 0 ? num_sms : 148);
+  while (bps > 4) {
+    const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((MB + bps - 1) / bps);
+    if (ctas >= want) break;
+    bps /= 2;
+  }
+  return bps;
+}
+
+size_t workspace_bytes_for(int64_t B, int64_t Hq, int64_t D, int64_t s_max) {
+  if (s_max <= 1) return 0;
+  const size_t acc = static_cast<size_t>(B * Hq * s_max * D) * 4;
+  const size_t ml = static_cast<size_t>(B * Hq * s_max * 2) * 4;
+  return ((acc + 255) & ~static_cast<size_t>(255)) + ml;
+}
+
+int nstage_default() {
+  static int v = [] {
+    const char* e = std::getenv("FORGE_PAGED_NSTAGE");
+    int n = e ? std::atoi(e) : 0;
+    return (n >= 2 && n <= 16) ? n : 8;
+  }();
+  return v;
+}
+
+int plan_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_tensor* v_cache,
+                const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                forge_tensor* out, int split_tokens, int num_sms, DecodePlan* plan) {
+  FORGE_TRY(check_tensor(q, FORGE_BF16, 3));
+  FORGE_TRY(check_cache(k_cache));
+  FORGE_TRY(check_cache(v_cache));
+  FORGE_TRY(check_tensor(block_tables, FORGE_I32, 2));
+  FORGE_TRY(check_tensor(context_lens, FORGE_I32, 1));
+  if (!out) return FORGE_ERR_NULL;
+  if (out->dtype != FORGE_BF16 && out->dtype != FORGE_F32) return FORGE_ERR_DTYPE;
+  if (out->ndim != 3) return FORGE_ERR_SHAPE;
+
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t NB = k_cache->shape[0], Hkv = k_cache->shape[1];
+  const int64_t MB = block_tables->shape[1];
+  for (int i = 0; i < 4; ++i)
+    if (v_cache->shape[i] != k_cache->shape[i]) return FORGE_ERR_SHAPE;
+  if (k_cache->shape[3] != D) return FORGE_ERR_SHAPE;
+  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D) return FORGE_ERR_SHAPE;
+  if (block_tables->shape[0] != B || context_lens->shape[0] != B) return FORGE_ERR_SHAPE;
+  if (B > 65535 || Hkv > 65535 || NB > INT32_MAX || MB > (INT32_MAX / kBlockSize)) return FORGE_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FORGE_ERR_UNSUPPORTED;
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return (Hkv <= 0 || Hq <= 0) ? FORGE_ERR_SHAPE : FORGE_ERR_UNSUPPORTED;
+  const int64_t G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return FORGE_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FORGE_ERR_VALUE;
+  if (split_tokens != 0 &&
+      (split_tokens < kMinSplitTokens || split_tokens > kMaxSplitTokens || split_tokens % kBlockSize != 0))
+    return FORGE_ERR_VALUE;
+
+  std::memset(plan, 0, sizeof(*plan));
+  plan->D = static_cast<int>(D);
+  plan->G = static_cast<int>(G);
+  plan->out_bf16 = out->dtype == FORGE_BF16;
+  if (B == 0) return FORGE_OK;
+
+  FORGE_TRY(check_vec16(q, 2));
+  FORGE_TRY(check_vec16(out, out->dtype == FORGE_BF16 ? 2 : 4));
+  if (!block_tables->data || !context_lens->data) return FORGE_ERR_NULL;
+  if (block_tables->stride[1] != 1 || context_lens->stride[0] != 1) return FORGE_ERR_SHAPE;
+  if (NB > 0 && (!k_cache->data || !v_cache->data)) return FORGE_ERR_NULL;
+
+  forge::DecodeParams& p = plan->p;
+  p.q = static_cast<const __nv_bfloat16*>(q->data);
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache->data);
+  p.v_cache = static_cast<const __nv_bfloat16*>(v_cache->data);
+  p.kc_sblk = k_cache->stride[0];
+  p.kc_sh = k_cache->stride[1];
+  p.vc_sblk = v_cache->stride[0];
+  p.vc_sh = v_cache->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_sb = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.out = out->data;
+  p.o_sb = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.B = static_cast<int>(B);
+  p.Hq = static_cast<int>(Hq);
+  p.Hkv = static_cast<int>(Hkv);
+  p.NB = static_cast<int>(NB);
+  p.MB = static_cast<int>(MB);
+  p.bps = split_blocks_for(split_tokens, p.B, p.Hkv, p.MB, num_sms);
+  p.s_max = MB > 0 ? static_cast<int>((MB + p.bps - 1) / p.bps) : 1;
+  p.nstage = nstage_default();
+  p.qk_scale_log2 = scale * 1.4426950408889634f;
+  plan->ws_bytes = workspace_bytes_for(B, Hq, D, p.s_max);
+  return FORGE_OK;
+}
+
+void attach_workspace(DecodePlan* plan, void* ws) {
+  forge::DecodeParams& p = plan->p;
+  if (plan->ws_bytes == 0) {
+    p.ws_acc = nullptr;
+    p.ws_ml = nullptr;
+    return;
+  }
+  const size_t acc = static_cast<size_t>(p.B) * p.Hq * p.s_max * plan->D * 4;
+  p.ws_acc = static_cast<float*>(ws);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((acc + 255) & ~static_cast<size_t>(255)));
+}
+
+int launch_plan(DecodePlan* plan, cudaStream_t stream) {
+  if (forge::launch_decode(plan->p, plan->D, plan->G, plan->out_bf16, stream) != cudaSuccess)
+    return FORGE_ERR_CUDA;
+  return FORGE_OK;
+}
+
+// Library-owned workspace for (device, stream), grown on demand.
+int cached_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto& slot = g_workspaces[{dev, stream}];
+  if (slot.second < bytes) {
+    if (slot.first) {
+      // the old buffer may still be in use by work queued on this stream
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return FORGE_ERR_CUDA;
+      cudaFree(slot.first);
+      slot = {nullptr, 0};
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return FORGE_ERR_CUDA;
+    slot = {p, bytes};
+  }
+  *out = slot.first;
+  return FORGE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int forge_paged_kv_append(const forge_tensor* k_new, const forge_tensor* v_new,
+                          const forge_tensor* slot_mapping, forge_tensor* k_cache,
+                          forge_tensor* v_cache, void* stream) {
+  FORGE_TRY(check_tensor(k_new, FORGE_BF16, 3));
+  FORGE_TRY(check_tensor(v_new, FORGE_BF16, 3));
+  FORGE_TRY(check_tensor(slot_mapping, FORGE_I64, 1));
+  FORGE_TRY(check_cache(k_cache));
+  FORGE_TRY(check_cache(v_cache));
+  const int64_t B = k_new->shape[0], Hkv = k_new->shape[1], D = k_new->shape[2];
+  for (int i = 0; i < 3; ++i)
+    if (v_new->shape[i] != k_new->shape[i]) return FORGE_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (v_cache->shape[i] != k_cache->shape[i]) return FORGE_ERR_SHAPE;
+  if (slot_mapping->shape[0] != B || k_cache->shape[1] != Hkv || k_cache->shape[3] != D) return FORGE_ERR_SHAPE;
+  if (D % 8 != 0) return FORGE_ERR_UNSUPPORTED;
+  if (B > INT32_MAX || Hkv > INT32_MAX || k_cache->shape[0] > INT32_MAX) return FORGE_ERR_UNSUPPORTED;
+  if (B == 0 || Hkv == 0 || D == 0) return FORGE_OK;
+  FORGE_TRY(check_vec16(k_new, 2));
+  FORGE_TRY(check_vec16(v_new, 2));
+  if (!slot_mapping->data) return FORGE_ERR_NULL;
+  if (slot_mapping->stride[0] != 1) return FORGE_ERR_SHAPE;
+  if (k_cache->shape[0] > 0 && (!k_cache->data || !v_cache->data)) return FORGE_ERR_NULL;
+
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+
+  forge::AppendParams p;
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new->data);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new->data);
+  p.kn_sb = k_new->stride[0];
+  p.kn_sh = k_new->stride[1];
+  p.vn_sb = v_new->stride[0];
+  p.vn_sh = v_new->stride[1];
+  p.slots = static_cast<const int64_t*>(slot_mapping->data);
+  p.k_cache = static_cast<__nv_bfloat16*>(k_cache->data);
+  p.v_cache = static_cast<__nv_bfloat16*>(v_cache->data);
+  p.kc_sblk = k_cache->stride[0];
+  p.kc_sh = k_cache->stride[1];
+  p.vc_sblk = v_cache->stride[0];
+  p.vc_sh = v_cache->stride[1];
+  p.B = static_cast<int>(B);
+  p.Hkv = static_cast<int>(Hkv);
+  p.D = static_cast<int>(D);
+  p.NB = static_cast<int>(k_cache->shape[0]);
+  p.err = err;
+  if (forge::launch_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FORGE_ERR_CUDA;
+  return FORGE_OK;
+}
+
+size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                              int split_tokens) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_blocks_per_seq < 0) return 0;
+  if (split_tokens != 0 &&
+      (split_tokens < kMinSplitTokens || split_tokens > kMaxSplitTokens || split_tokens % kBlockSize != 0))
+    return 0;
+  // The automatic split length depends on the SM count; plan for the
+  // smallest split it can pick so the size is an upper bound.
+  const int bps = split_tokens ? split_tokens / kBlockSize : 4;
+  const int64_t s_max = max_blocks_per_seq > 0 ? (max_blocks_per_seq + bps - 1) / bps : 1;
+  return workspace_bytes_for(B, Hq, D, s_max);
+}
+
+int forge_paged_gqa_decode_ex(const forge_tensor* q, const forge_tensor* k_cache, const forge_tensor* v_cache,
+                              const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                              forge_tensor* out, void* workspace, size_t workspace_bytes, int split_tokens,
+                              void* stream) {
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  DecodePlan plan;
+  FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, split_tokens, 148, &plan));
+  if (plan.p.B == 0) return FORGE_OK;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+  if (split_tokens == 0) {  // re-plan with the real SM count
+    FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, sms, &plan));
+  }
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return FORGE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FORGE_ERR_ALIGN;
+  }
+  plan.p.err = err;
+  attach_workspace(&plan, workspace);
+  return launch_plan(&plan, static_cast<cudaStream_t>(stream));
+}
+
+int forge_paged_gqa_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_tensor* v_cache,
+                           const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                           forge_tensor* out, void* stream) {
+  DecodePlan plan;
+  FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, 148, &plan));
+  if (plan.p.B == 0) return FORGE_OK;
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+  FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, sms, &plan));
+  void* ws = nullptr;
+  if (plan.ws_bytes > 0) FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws));
+  plan.p.err = err;
+  attach_workspace(&plan, ws);
+  return launch_plan(&plan, static_cast<cudaStream_t>(stream));
+}
+
+const char* forge_status_string(int status) {
+  switch (status) {
+    case FORGE_OK: return "FORGE_OK";
+    case FORGE_ERR_NULL: return "FORGE_ERR_NULL: a descriptor or needed data pointer is NULL";
+    case FORGE_ERR_DTYPE: return "FORGE_ERR_DTYPE: wrong dtype";
+    case FORGE_ERR_SHAPE: return "FORGE_ERR_SHAPE: wrong rank, mismatched sizes or unsupported strides";
+    case FORGE_ERR_UNSUPPORTED: return "FORGE_ERR_UNSUPPORTED: head size, block size or group size not built";
+    case FORGE_ERR_ALIGN: return "FORGE_ERR_ALIGN: pointer or stride breaks 16-byte alignment";
+    case FORGE_ERR_CUDA: return "FORGE_ERR_CUDA: a CUDA call or launch failed";
+    case FORGE_ERR_WORKSPACE: return "FORGE_ERR_WORKSPACE: workspace missing or too small";
+    case FORGE_ERR_VALUE: return "FORGE_ERR_VALUE: scalar argument out of range";
+    default: return "unknown forge status";
+  }
+}
+
+int forge_paged_get_device_error(void* stream, int* code_out) {
+  if (!code_out) return FORGE_ERR_NULL;
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FORGE_ERR_CUDA;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FORGE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FORGE_ERR_CUDA;
+  *code_out = host;
+  return FORGE_OK;
+}
+
+const char* forge_paged_version(void) { return "0.1.0"; }
+
+}  // extern "C"

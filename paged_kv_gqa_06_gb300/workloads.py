@@ -19,8 +19,9 @@ Recipe (every config):
     seeded random permutation of range(NB), handed out to sequences in order;
     ids the permutation leaves over are free blocks scattered through the
     pool.  Unused block-table entries are -1.
-  * Values: float32 N(0, 1) draws from numpy's PCG64, rounded to bf16 with
-    round-to-nearest-even.  Config "qwen3_4b" doubles K (an exact power-of-two
+  * Values: float32 N(0, 1) draws from numpy's PCG64 (one stream per
+    4 Mi-element chunk, seeded by (seed, layer, tensor, chunk)), rounded to
+    bf16 with round-to-nearest-even.  Config "qwen3_4b" doubles K (an exact power-of-two
     scale) so that logits reach about +-8.
   * Poison: every cache slot that holds no token before the append -- free
     blocks, the tail of each sequence's last block, and the append target
@@ -31,6 +32,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -53,19 +55,40 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, shape, mul: float = 1.0) -> np.ndarray:
-    """bf16 bits of mul * N(0,1) (mul a power of two, so the scaling is exact)."""
+_CHUNK = 1 << 22
+_pool = None
+
+
+def _threads():
+    global _pool
+    if _pool is None:
+        from concurrent.futures import ThreadPoolExecutor
+        _pool = ThreadPoolExecutor(max_workers=max(1, min(16, len(os.sched_getaffinity(0)))))
+    return _pool
+
+
+def _normal_bf16(key, shape, mul: float = 1.0) -> np.ndarray:
+    """bf16 bits of mul * N(0,1) (mul a power of two, so the scaling is exact).
+
+    Chunk c of the array draws from its own PCG64 stream seeded by
+    (*key, c), so the values do not depend on how many threads fill it.
+    """
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    chunk = 1 << 22
-    buf = np.empty(min(n, chunk), dtype=np.float32)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        view = buf[: e - s]
-        rng.standard_normal(out=view, dtype=np.float32)
+
+    def fill(c):
+        s, e = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        x = np.random.default_rng([*key, c]).standard_normal(e - s, dtype=np.float32)
         if mul != 1.0:
-            view *= np.float32(mul)
-        out[s:e] = f32_to_bf16_bits(view)
+            x *= np.float32(mul)
+        out[s:e] = f32_to_bf16_bits(x)
+
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        list(_threads().map(fill, range(nchunks)))
     return out.reshape(shape)
 
 
@@ -159,13 +182,13 @@ class Workload:
     def layer(self, l: int = 0) -> dict:
         """q, k_new, v_new and the pre-append (poisoned) caches of layer ``l``."""
         s = self.spec
-        rng = np.random.default_rng([self.seed, 1 + l])
-        q = _normal_bf16(rng, (s.B, s.Hq, s.D))
-        k_new = _normal_bf16(rng, (s.B, s.Hkv, s.D), s.k_mul)
-        v_new = _normal_bf16(rng, (s.B, s.Hkv, s.D))
+        key = (self.seed, 1 + l)
+        q = _normal_bf16((*key, 0), (s.B, s.Hq, s.D))
+        k_new = _normal_bf16((*key, 1), (s.B, s.Hkv, s.D), s.k_mul)
+        v_new = _normal_bf16((*key, 2), (s.B, s.Hkv, s.D))
         shape = (self.NB, s.Hkv, BLOCK_SIZE, s.D)
-        k_cache = _normal_bf16(rng, shape, s.k_mul)
-        v_cache = _normal_bf16(rng, shape)
+        k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
+        v_cache = _normal_bf16((*key, 4), shape)
         pb, po = np.nonzero(self.poison_mask())
         k_cache[pb, :, po, :] = BF16_NAN
         v_cache[pb, :, po, :] = BF16_NAN

@@ -1,0 +1,150 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+entry point include/forge_paged.h declares, and rejects bad arguments on the
+host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_gqa_06_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "forge_paged.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_gqa_06_gb300 import build
+    build.build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FORGE_API\s+[\w\s\*]*?\b(forge_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in forge_paged.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    for code in range(-8, 1):
+        assert lib.forge_status_string(code)
+    assert lib.forge_status_string(-99) == b"unknown forge status"
+    assert lib.forge_paged_version() == b"0.1.0"
+
+
+def test_workspace_bytes_is_host_only(lib):
+    f = binding.forge_paged_gqa_decode_workspace_bytes
+    assert f(32, 32, 8, 128, 512, 512) == ((32 * 32 * 16 * 128 * 4 + 255) // 256) * 256 + 32 * 32 * 16 * 2 * 4
+    assert f(4, 8, 2, 64, 4, 1024) == 0      # one split: no scratch
+    assert f(4, 8, 2, 64, 4, 17) == 0        # invalid split length
+    assert f(-1, 8, 2, 64, 4, 0) == 0
+
+
+def _desc(shape, dtype, data=16, stride=None):
+    d = binding.ForgeTensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    st = stride
+    if st is None:
+        st, acc = [], 1
+        for s in reversed(shape):
+            st.insert(0, acc)
+            acc *= s
+    for i, s in enumerate(shape):
+        d.shape[i] = s
+        d.stride[i] = st[i]
+    return d
+
+
+BF16, F32, I32, I64 = binding.FORGE_BF16, binding.FORGE_F32, binding.FORGE_I32, binding.FORGE_I64
+
+
+def _decode_args(**over):
+    B, Hq, Hkv, D, NB, MB = 2, 8, 2, 64, 8, 4
+    a = dict(q=_desc([B, Hq, D], BF16), k=_desc([NB, Hkv, 16, D], BF16), v=_desc([NB, Hkv, 16, D], BF16),
+             bt=_desc([B, MB], I32), cl=_desc([B], I32), scale=0.125, out=_desc([B, Hq, D], F32))
+    a.update(over)
+    return a
+
+
+def _call_decode(lib, a):
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    return lib.forge_paged_gqa_decode(r(a["q"]), r(a["k"]), r(a["v"]), r(a["bt"]), r(a["cl"]), a["scale"],
+                                      r(a["out"]), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), -1),
+    (dict(q=_desc([2, 8, 64], F32)), -2),
+    (dict(q=_desc([2, 8, 64, 1], BF16)), -3),
+    (dict(out=_desc([2, 8, 64], I32)), -2),
+    (dict(out=_desc([2, 4, 64], F32)), -3),
+    (dict(k=_desc([8, 2, 8, 64], BF16), v=_desc([8, 2, 8, 64], BF16)), -4),     # block size 8
+    (dict(q=_desc([2, 8, 96], BF16), k=_desc([8, 2, 16, 96], BF16), v=_desc([8, 2, 16, 96], BF16),
+          out=_desc([2, 8, 96], F32)), -4),                                        # D = 96
+    (dict(q=_desc([2, 6, 64], BF16), out=_desc([2, 6, 64], F32)), -4),             # Hq % Hkv != 0
+    (dict(q=_desc([2, 32, 64], BF16), out=_desc([2, 32, 64], F32)), -4),           # G = 16
+    (dict(bt=_desc([3, 4], I32)), -3),
+    (dict(cl=_desc([2], I64)), -2),
+    (dict(scale=float("nan")), -8),
+    (dict(q=_desc([2, 8, 64], BF16, data=8)), -5),                                 # misaligned
+    (dict(q=_desc([2, 8, 64], BF16, stride=[512, 60, 1])), -5),                    # stride not x8
+    (dict(q=_desc([2, 8, 64], BF16, stride=[1, 128, 2])), -3),                     # inner stride
+    (dict(k=_desc([8, 2, 16, 64], BF16, stride=[4096, 2048, 65, 1])), -3),        # tile not contiguous
+    (dict(v=_desc([8, 4, 16, 64], BF16)), -3),
+])
+def test_decode_rejects_bad_arguments(lib, over, status):
+    assert _call_decode(lib, _decode_args(**over)) == status
+
+
+def test_decode_with_valid_arguments_reaches_cuda(lib):
+    rc = _call_decode(lib, _decode_args())
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU tests cover real calls")
+    assert rc == -6        # no device here: the first CUDA call fails cleanly
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _decode_args(q=_desc([0, 8, 64], BF16, data=0), bt=_desc([0, 4], I32, data=0), cl=_desc([0], I32, data=0),
+                     out=_desc([0, 8, 64], F32, data=0))
+    assert _call_decode(lib, a) == 0
+
+
+def _call_append(lib, kn, vn, sm, kc, vc):
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    return lib.forge_paged_kv_append(r(kn), r(vn), r(sm), r(kc), r(vc), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(kn=None), -1),
+    (dict(sm=_desc([2], I32)), -2),
+    (dict(sm=_desc([3], I64)), -3),
+    (dict(kn=_desc([2, 2, 64], F32)), -2),
+    (dict(kc=_desc([8, 2, 32, 64], BF16)), -4),
+    (dict(kn=_desc([2, 2, 64], BF16, data=4)), -5),
+    (dict(vn=_desc([2, 3, 64], BF16)), -3),
+])
+def test_append_rejects_bad_arguments(lib, over, status):
+    a = dict(kn=_desc([2, 2, 64], BF16), vn=_desc([2, 2, 64], BF16), sm=_desc([2], I64),
+             kc=_desc([8, 2, 16, 64], BF16), vc=_desc([8, 2, 16, 64], BF16))
+    a.update(over)
+    assert _call_append(lib, a["kn"], a["vn"], a["sm"], a["kc"], a["vc"]) == status
+
+
+def test_python_binding_raises_on_bad_status(lib):
+    q = torch.zeros(2, 8, 96, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 96, dtype=torch.bfloat16)
+    out = torch.zeros(2, 8, 96)
+    with pytest.raises(binding.ForgeError) as e:
+        binding.forge_paged_gqa_decode(q, kc, kc, torch.zeros(2, 4, dtype=torch.int32),
+                                       torch.zeros(2, dtype=torch.int32), 0.1, out, stream=0)
+    assert e.value.status == -4
