@@ -376,7 +376,8 @@ def run_native(args, wl, out_bytes):
                                           f"{2 * k_cache.numel() * 2 / 1e6:.0f} MB vs 126 MB L2)",
                                     "bytes_per_step": bytes_step,
                                     "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
-        "roofline": {"bound": "hbm", "kernel": "forge_paged_gqa_decode (split kernel + split reduce)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "paged_gqa_decode_split_kernel, timed with its split reduce (one decode call)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),

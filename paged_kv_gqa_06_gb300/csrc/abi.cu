@@ -132,7 +132,7 @@ int nstage_default() {
   static int v = [] {
     const char* e = std::getenv("FORGE_PAGED_NSTAGE");
     int n = e ? std::atoi(e) : 0;
-    return (n >= 2 && n <= 16) ? n : 8;
+    return (n >= 2 && n <= 16) ? n : 4;
   }();
   return v;
 }

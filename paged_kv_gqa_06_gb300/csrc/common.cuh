@@ -53,7 +53,7 @@ struct DecodeParams {
   int B, Hq, Hkv, NB, MB;
   int bps;         // KV blocks per split
   int s_max;       // split slots per (b, h) in the workspace
-  int nstage;      // shared-memory ring depth (tiles)
+  int nstage;      // shared-memory ring depth (pipeline stages)
   float qk_scale_log2;  // scale * log2(e): logits come out in log2 units
   int* err;
 };
@@ -143,6 +143,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // bf16 pair (low element in bits 0..15) -> two floats, exactly.
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// d = a * b + c on both lanes of a float pair with one packed fp32 FMA
+// (sm_100-family f32x2 instruction; each lane rounds like a scalar fmaf).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
 
 // Launchers (defined in append.cu / decode.cu).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

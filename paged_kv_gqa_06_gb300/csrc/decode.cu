@@ -13,14 +13,17 @@
 //     `bps` consecutive KV blocks of one sequence; every K/V byte is read once
 //     and used for all G query heads of its group;
 //   * warp 4 is the producer: it translates logical blocks through the block
-//     table and streams each (block, head) K tile, then each V tile (16 x D
-//     bf16, one contiguous run) into a ring of shared-memory slots with
-//     single bulk copies on the TMA engine, tracked by mbarriers;
-//   * warps 0-3 consume: 8 lanes per token, D/8 dims per lane.  Pass 1 forms
-//     the G logits of every token of the split (fp32 FMA on bf16 widened
-//     exactly, 3-step shuffle reduction) into shared memory; the split's max
-//     and sum are taken over all of them at once (no running rescale); pass 2
-//     accumulates p * V in registers;
+//     table and streams the split's K tiles, then its V tiles, into a ring of
+//     shared-memory stages.  A stage holds two (block, head) tiles (16 x D
+//     bf16 each, one contiguous run apiece), moved by single bulk copies on
+//     the TMA engine and tracked by one mbarrier;
+//   * warps 0-3 consume: 8 lanes per token, D/8 dims per lane, two tokens
+//     per thread per stage.  Pass 1 forms the G logits of every token of the
+//     split (packed fp32x2 FMA on bf16 widened exactly) and sums each 8-lane
+//     group with a transposing shuffle reduction that ends with one (token,
+//     head) logit per lane; the split's max and sum are then taken over all
+//     logits at once (no running rescale); pass 2 accumulates p * V in
+//     registers;
 //   * a split that is the whole sequence writes `out` directly; otherwise it
 //     writes unnormalised (acc, max, sum) and the reduce kernel merges the
 //     splits of each (b, h).
@@ -40,20 +43,26 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kStageBlocks = 2;            // KV blocks per pipeline stage
+constexpr int kGroups = kConsumers / 8;    // token groups (8 lanes each)
 
 struct SmemLayout {
-  size_t ring, logits, red_acc, red_ml, bars, total;
+  size_t ring, logits, red_ml, bars, total;
 };
 
+// ring: nstage stages of kStageBlocks tiles; reused at the end for the
+// cross-group sum, [kGroups][G][D] fp32.  logits: [bps*16][G] fp32 (rounded
+// up to whole stages).
 __host__ __device__ inline SmemLayout decode_layout(int D, int G, int bps, int nstage) {
   SmemLayout l;
   size_t off = 0;
   l.ring = off;
-  off += static_cast<size_t>(nstage) * kBlockSize * D * 2;
+  const size_t ring = static_cast<size_t>(nstage) * kStageBlocks * kBlockSize * D * 2;
+  const size_t red = static_cast<size_t>(kGroups) * G * D * 4;
+  off += ring > red ? ring : red;
   l.logits = off;
-  off += static_cast<size_t>(bps) * kBlockSize * G * 4;
-  l.red_acc = off;
-  off += static_cast<size_t>(kConsumerWarps) * G * D * 4;
+  const int bps_up = (bps + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
+  off += static_cast<size_t>(bps_up) * kBlockSize * G * 4;
   l.red_ml = off;
   off += static_cast<size_t>(2) * kConsumerWarps * G * 4;
   off = (off + 15) & ~static_cast<size_t>(15);
@@ -111,14 +120,55 @@ __device__ __forceinline__ int checked_length(const DecodeParams& p, int b, bool
   return L;
 }
 
+// Sum each of a lane's CNT values over the 8 lanes of its token group (lanes
+// that differ in bits 0..2).  At each exchange step a lane keeps one half of
+// the values it still holds and hands the other half to its partner, so the
+// shuffle count halves per step.  Afterwards lane `sub` holds the group sums
+// of values [first, first + max(N/8, 1)), returned in v[0..].
+template <int CNT, int M>
+struct Group8Sum {
+  template <int N>
+  static __device__ __forceinline__ void run(float (&v)[N], int sub, int& first) {
+    const bool hi = (sub & M) != 0;
+    if constexpr (CNT > 1) {
+      constexpr int H = CNT / 2;
+#pragma unroll
+      for (int k = 0; k < H; ++k) {
+        const float keep = hi ? v[H + k] : v[k];
+        const float send = hi ? v[k] : v[H + k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+      }
+      if (hi) first += H;
+      if constexpr (M > 1) Group8Sum<H, M / 2>::run(v, sub, first);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+      if constexpr (M > 1) Group8Sum<1, M / 2>::run(v, sub, first);
+    }
+  }
+};
+
+// Load one token row slice: chunk c (16 bytes) of this lane sits at element
+// c * 64 + sub * 8, so the 8 lanes of a token read 128 contiguous bytes per
+// chunk (no shared-memory bank conflicts).
+template <int D>
+__device__ __forceinline__ void load_row_slice(const __nv_bfloat16* row, int sub, uint32_t (&w)[D / 16]) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint4 x = *reinterpret_cast<const uint4*>(row + c * 64 + sub * 8);
+    w[4 * c] = x.x;
+    w[4 * c + 1] = x.y;
+    w[4 * c + 2] = x.z;
+    w[4 * c + 3] = x.w;
+  }
+}
+
 template <int D, int G, typename OutT>
-__global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const DecodeParams p) {
-  constexpr int DPL = D / 8;   // dims per lane (8 lanes per token)
-  constexpr int WPL = DPL / 2; // bf16 pairs per lane
-  constexpr int VEC = DPL / 8; // 16-byte vectors per lane
+__global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_split_kernel(const DecodeParams p) {
+  constexpr int WPL = D / 16;  // bf16 pairs per lane per token row
   constexpr int TILE = kBlockSize * D;
   constexpr uint32_t kTileBytes = TILE * sizeof(__nv_bfloat16);
-  static_assert(D % 64 == 0, "8 lanes x whole 16-byte vectors per token row");
+  constexpr int NV = kStageBlocks * G;  // logits a thread forms per stage
+  static_assert(D % 64 == 0, "8 lanes x whole 16-byte chunks per token row");
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,14 +189,15 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   if (s >= nsplit) return;
 
   const int blk0 = s * p.bps;
-  const int n = min(p.bps, nblk - blk0);  // KV blocks in this split (>= 1)
+  const int n = min(p.bps, nblk - blk0);                    // KV blocks in this split (>= 1)
+  const int nks = (n + kStageBlocks - 1) / kStageBlocks;    // stages per pass
   const int nstage = p.nstage;
 
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout lay = decode_layout(D, G, p.bps, nstage);
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem + lay.ring);
+  float* red = reinterpret_cast<float*>(smem + lay.ring);  // reuses the ring at the end
   float* logits = reinterpret_cast<float*>(smem + lay.logits);
-  float* red_acc = reinterpret_cast<float*>(smem + lay.red_acc);
   float* red_m = reinterpret_cast<float*>(smem + lay.red_ml);
   float* red_l = red_m + kConsumerWarps * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
@@ -173,19 +224,33 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     const __nv_bfloat16* vbase = p.v_cache + g * p.vc_sh;
     int slot = 0;
     uint32_t phase = 0;
-    for (int i = 0; i < 2 * n; ++i) {
-      const bool is_v = i >= n;
-      const int j = is_v ? i - n : i;
-      const int pb = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
+    for (int i = 0; i < 2 * nks; ++i) {
+      const bool is_v = i >= nks;
+      const int j0 = (is_v ? i - nks : i) * kStageBlocks;
+      int pb[kStageBlocks];
+#pragma unroll
+      for (int u = 0; u < kStageBlocks; ++u) {
+        const int j = j0 + u;  // <= 63 < 2 * 32
+        pb[u] = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
+        if (j >= n) pb[u] = -1;  // past the split: no tile
+      }
       if (lane == 0) {
-        if (i >= nstage) mbar_wait(empty + slot, phase ^ 1u, p.err);  // slot released
-        if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.NB)) {
-          const __nv_bfloat16* src =
-              is_v ? vbase + static_cast<int64_t>(pb) * p.vc_sblk : kbase + static_cast<int64_t>(pb) * p.kc_sblk;
-          mbar_arrive_expect_tx(full + slot, kTileBytes);
-          bulk_copy_g2s(ring + slot * TILE, src, kTileBytes, full + slot);
+        if (i >= nstage) mbar_wait(empty + slot, phase ^ 1u, p.err);  // stage released
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int u = 0; u < kStageBlocks; ++u)
+          if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += kTileBytes;
+        if (bytes) {
+          mbar_arrive_expect_tx(full + slot, bytes);
+          const __nv_bfloat16* base = is_v ? vbase : kbase;
+          const int64_t sblk = is_v ? p.vc_sblk : p.kc_sblk;
+#pragma unroll
+          for (int u = 0; u < kStageBlocks; ++u)
+            if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB))
+              bulk_copy_g2s(ring + (slot * kStageBlocks + u) * TILE, base + static_cast<int64_t>(pb[u]) * sblk,
+                            kTileBytes, full + slot);
         } else {
-          mbar_arrive(full + slot);  // bad block id (recorded): release the slot without data
+          mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
         }
       }
       if (++slot == nstage) {
@@ -198,25 +263,21 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
 
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
-  const int tok = tid >> 3;     // token of the tile this thread reads
+  const int tok = tid >> 3;     // token row within each tile of a stage
   const int sub = tid & 7;
-  const int d0 = sub * DPL;
   const int t_base = blk0 * kBlockSize;
 
-  float qf[G][DPL];
+  // q of the G heads of this group, prescaled into log2 units, as float pairs
+  // in this lane's dims {c*64 + sub*8 + e}.
+  float2 q2[G][WPL];
 #pragma unroll
   for (int i = 0; i < G; ++i) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(b) * p.q_sb +
-                                                      static_cast<int64_t>(g * G + i) * p.q_sh + d0);
+    uint32_t w[WPL];
+    load_row_slice<D>(p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + i) * p.q_sh, sub, w);
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      const uint4 w4 = __ldg(src + v);
-      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        qf[i][8 * v + 2 * k] = bf16lo(w[k]) * p.qk_scale_log2;
-        qf[i][8 * v + 2 * k + 1] = bf16hi(w[k]) * p.qk_scale_log2;
-      }
+    for (int k = 0; k < WPL; ++k) {
+      const float2 f = bf16x2_to_float2(w[k]);
+      q2[i][k] = make_float2(f.x * p.qk_scale_log2, f.y * p.qk_scale_log2);
     }
   }
 
@@ -224,46 +285,44 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   uint32_t phase = 0;
 
   // ---- pass 1: logits of every token of the split (log2 units)
-  for (int j = 0; j < n; ++j) {
+  for (int st = 0; st < nks; ++st) {
     mbar_wait(full + slot, phase, p.err);
-    uint32_t kw[WPL];
-    const uint4* src = reinterpret_cast<const uint4*>(ring + slot * TILE + tok * D + d0);
+    float v[NV];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      const uint4 x = src[v];
-      kw[4 * v] = x.x;
-      kw[4 * v + 1] = x.y;
-      kw[4 * v + 2] = x.z;
-      kw[4 * v + 3] = x.w;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + slot);
-
-    float part[G];
-#pragma unroll
-    for (int i = 0; i < G; ++i) part[i] = 0.f;
-#pragma unroll
-    for (int w = 0; w < WPL; ++w) {
-      const float k0 = bf16lo(kw[w]), k1 = bf16hi(kw[w]);
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        part[i] = fmaf(qf[i][2 * w], k0, part[i]);
-        part[i] = fmaf(qf[i][2 * w + 1], k1, part[i]);
+    for (int u = 0; u < kStageBlocks; ++u) {
+      uint32_t kw[WPL];
+      load_row_slice<D>(ring + (slot * kStageBlocks + u) * TILE + tok * D, sub, kw);
+      if (u == kStageBlocks - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
       }
-    }
+      float2 acc[G];
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      part[i] += __shfl_xor_sync(0xffffffffu, part[i], 1);
-      part[i] += __shfl_xor_sync(0xffffffffu, part[i], 2);
-      part[i] += __shfl_xor_sync(0xffffffffu, part[i], 4);
-    }
-    if (sub == 0) {
-      const bool valid = t_base + j * kBlockSize + tok < L;
-      if (!valid) {
+      for (int i = 0; i < G; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < G; ++i) part[i] = -INFINITY;
+      for (int k = 0; k < WPL; ++k) {
+        const float2 kf = bf16x2_to_float2(kw[k]);
+#pragma unroll
+        for (int i = 0; i < G; ++i) acc[i] = ffma2(q2[i][k], kf, acc[i]);
       }
-      store_row<G>(logits + (j * kBlockSize + tok) * G, part);
+#pragma unroll
+      for (int i = 0; i < G; ++i) v[u * G + i] = acc[i].x + acc[i].y;
+    }
+    int first = 0;
+    Group8Sum<NV, 4>::run(v, sub, first);
+    constexpr int kOut = NV >= 8 ? NV / 8 : 1;
+    constexpr int kDup = NV >= 8 ? 1 : 8 / NV;  // lanes holding the same sum
+    if ((sub & (kDup - 1)) == 0) {
+#pragma unroll
+      for (int k = 0; k < kOut; ++k) {
+        const int idx = first + k;
+        const int u = idx / G, i = idx % G;
+        const int j = st * kStageBlocks + u;  // block within the split
+        if (j < n) {
+          const bool valid = t_base + j * kBlockSize + tok < L;
+          logits[(j * kBlockSize + tok) * G + i] = valid ? v[k] : -INFINITY;
+        }
+      }
     }
     if (++slot == nstage) {
       slot = 0;
@@ -274,16 +333,15 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
 
   // ---- softmax over the split: max, then p = 2^(s - max) in place, and sum
   const int ntok = n * kBlockSize;
-  float m[G];
   {
     float mx[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) mx[i] = -INFINITY;
     for (int t = tid; t < ntok; t += kConsumers) {
-      float v[G];
-      load_row<G>(logits + t * G, v);
+      float x[G];
+      load_row<G>(logits + t * G, x);
 #pragma unroll
-      for (int i = 0; i < G; ++i) mx[i] = fmaxf(mx[i], v[i]);
+      for (int i = 0; i < G; ++i) mx[i] = fmaxf(mx[i], x[i]);
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -295,6 +353,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
       for (int i = 0; i < G; ++i) red_m[warp * G + i] = mx[i];
     }
     named_barrier(1, kConsumers);
+    float m[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       m[i] = red_m[i];
@@ -305,14 +364,14 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
 #pragma unroll
     for (int i = 0; i < G; ++i) sum[i] = 0.f;
     for (int t = tid; t < ntok; t += kConsumers) {
-      float v[G];
-      load_row<G>(logits + t * G, v);
+      float x[G];
+      load_row<G>(logits + t * G, x);
 #pragma unroll
       for (int i = 0; i < G; ++i) {
-        v[i] = fast_exp2(v[i] - m[i]);
-        sum[i] += v[i];
+        x[i] = fast_exp2(x[i] - m[i]);
+        sum[i] += x[i];
       }
-      store_row<G>(logits + t * G, v);
+      store_row<G>(logits + t * G, x);
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
@@ -327,36 +386,31 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   }
 
   // ---- pass 2: acc += p * V over this thread's tokens
-  float acc[G][DPL];
+  float2 acc[G][WPL];
 #pragma unroll
   for (int i = 0; i < G; ++i)
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[i][k] = 0.f;
+    for (int k = 0; k < WPL; ++k) acc[i][k] = make_float2(0.f, 0.f);
 
-  for (int j = 0; j < n; ++j) {
+  for (int st = 0; st < nks; ++st) {
     mbar_wait(full + slot, phase, p.err);
-    uint32_t vw[WPL];
-    const uint4* src = reinterpret_cast<const uint4*>(ring + slot * TILE + tok * D + d0);
+    uint32_t vw[kStageBlocks][WPL];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      const uint4 x = src[v];
-      vw[4 * v] = x.x;
-      vw[4 * v + 1] = x.y;
-      vw[4 * v + 2] = x.z;
-      vw[4 * v + 3] = x.w;
-    }
+    for (int u = 0; u < kStageBlocks; ++u)
+      load_row_slice<D>(ring + (slot * kStageBlocks + u) * TILE + tok * D, sub, vw[u]);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + slot);
-    if (t_base + j * kBlockSize + tok < L) {
-      float w[G];
-      load_row<G>(logits + (j * kBlockSize + tok) * G, w);
 #pragma unroll
-      for (int ww = 0; ww < WPL; ++ww) {
-        const float v0 = bf16lo(vw[ww]), v1 = bf16hi(vw[ww]);
+    for (int u = 0; u < kStageBlocks; ++u) {
+      const int j = st * kStageBlocks + u;
+      if (j < n && t_base + j * kBlockSize + tok < L) {
+        float w[G];
+        load_row<G>(logits + (j * kBlockSize + tok) * G, w);
 #pragma unroll
-        for (int i = 0; i < G; ++i) {
-          acc[i][2 * ww] = fmaf(w[i], v0, acc[i][2 * ww]);
-          acc[i][2 * ww + 1] = fmaf(w[i], v1, acc[i][2 * ww + 1]);
+        for (int k = 0; k < WPL; ++k) {
+          const float2 vf = bf16x2_to_float2(vw[u][k]);
+#pragma unroll
+          for (int i = 0; i < G; ++i) acc[i][k] = ffma2(make_float2(w[i], w[i]), vf, acc[i][k]);
         }
       }
     }
@@ -366,59 +420,67 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     }
   }
 
-  // ---- combine the 16 token groups: lanes 8 and 16 apart, then the 4 warps
+  // ---- combine the kGroups token groups through shared memory (the ring is
+  // free: every stage has been consumed by all consumer warps)
+  named_barrier(1, kConsumers);
 #pragma unroll
   for (int i = 0; i < G; ++i)
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) {
-      acc[i][k] += __shfl_xor_sync(0xffffffffu, acc[i][k], 8);
-      acc[i][k] += __shfl_xor_sync(0xffffffffu, acc[i][k], 16);
+    for (int c = 0; c < D / 64; ++c) {
+      float4* dst = reinterpret_cast<float4*>(red + (tok * G + i) * D + c * 64 + sub * 8);
+      dst[0] = make_float4(acc[i][4 * c].x, acc[i][4 * c].y, acc[i][4 * c + 1].x, acc[i][4 * c + 1].y);
+      dst[1] = make_float4(acc[i][4 * c + 2].x, acc[i][4 * c + 2].y, acc[i][4 * c + 3].x, acc[i][4 * c + 3].y);
     }
-  if (lane < 8) {
-#pragma unroll
-    for (int i = 0; i < G; ++i)
-#pragma unroll
-      for (int k = 0; k < DPL; k += 4)
-        *reinterpret_cast<float4*>(red_acc + (warp * G + i) * D + d0 + k) =
-            make_float4(acc[i][k], acc[i][k + 1], acc[i][k + 2], acc[i][k + 3]);
-  }
   named_barrier(1, kConsumers);
 
-  float l[G];
+  for (int o = tid * 4; o < G * D; o += kConsumers * 4) {
+    const int i = o / D, d = o % D;
+    float4 t = *reinterpret_cast<const float4*>(red + i * D + d);
 #pragma unroll
-  for (int i = 0; i < G; ++i) {
-    l[i] = red_l[i];
+    for (int grp = 1; grp < kGroups; ++grp) {
+      const float4 x = *reinterpret_cast<const float4*>(red + (grp * G + i) * D + d);
+      t.x += x.x;
+      t.y += x.y;
+      t.z += x.z;
+      t.w += x.w;
+    }
+    // the split's sum for head i: total of the per-warp sums
+    float li = red_l[i];
 #pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) l[i] += red_l[w * G + i];
-  }
-#pragma unroll
-  for (int i = 0; i < G; ++i) {
+    for (int w = 1; w < kConsumerWarps; ++w) li += red_l[w * G + i];
     const int h = g * G + i;
-    for (int d = tid; d < D; d += kConsumers) {
-      float v = red_acc[i * D + d];
+    if (nsplit == 1) {
+      OutT* dst = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + h * p.o_sh + d;
+      store_out(dst + 0, t.x / li);
+      store_out(dst + 1, t.y / li);
+      store_out(dst + 2, t.z / li);
+      store_out(dst + 3, t.w / li);
+    } else {
+      *reinterpret_cast<float4*>(p.ws_acc + ((static_cast<int64_t>(b) * p.Hq + h) * p.s_max + s) * D + d) = t;
+    }
+  }
+  if (nsplit > 1 && tid < G) {
+    float mi = red_m[tid], li = red_l[tid];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) v += red_acc[(w * G + i) * D + d];
-      if (nsplit == 1) {
-        store_out(reinterpret_cast<OutT*>(p.out) + b * p.o_sb + h * p.o_sh + d, v / l[i]);
-      } else {
-        p.ws_acc[((static_cast<int64_t>(b) * p.Hq + h) * p.s_max + s) * D + d] = v;
-      }
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      mi = fmaxf(mi, red_m[w * G + tid]);
+      li += red_l[w * G + tid];
     }
-    if (nsplit > 1 && tid == i) {
-      const int64_t r = (static_cast<int64_t>(b) * p.Hq + h) * p.s_max + s;
-      p.ws_ml[2 * r] = m[i];
-      p.ws_ml[2 * r + 1] = l[i];
-    }
+    const int64_t r = (static_cast<int64_t>(b) * p.Hq + g * G + tid) * p.s_max + s;
+    p.ws_ml[2 * r] = mi;
+    p.ws_ml[2 * r + 1] = li;
   }
 }
 
 // Merge the split partials of every (b, h) whose sequence has more than one
 // split: with M = max_s m_s and w_s = 2^(m_s - M),
 //   out = sum_s w_s acc_s / sum_s w_s l_s.
-// One warp per (b, h); each lane owns D/32 consecutive dims.
+// One warp per (b, h); each lane owns D/32 consecutive dims.  The split loop
+// is unrolled by 8 so that eight partial rows are in flight at once.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(128) paged_gqa_decode_reduce_kernel(const DecodeParams p) {
   constexpr int DPT = D / 32;
+  constexpr int U = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rowid = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (rowid >= static_cast<int64_t>(p.B) * p.Hq) return;
@@ -442,19 +504,36 @@ __global__ void __launch_bounds__(128) paged_gqa_decode_reduce_kernel(const Deco
 #pragma unroll
   for (int k = 0; k < DPT; ++k) acc[k] = 0.f;
   const float* a = p.ws_acc + rowid * p.s_max * D + lane * DPT;
-  for (int s = 0; s < nsplit; ++s) {
-    const float w = fast_exp2(ml[2 * s] - M);
-    if constexpr (DPT == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(a + static_cast<int64_t>(s) * D);
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
-      acc[2] = fmaf(w, x.z, acc[2]);
-      acc[3] = fmaf(w, x.w, acc[3]);
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(a + static_cast<int64_t>(s) * D);
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
+  int s = 0;
+  for (; s + U <= nsplit; s += U) {
+    float x[U][DPT], w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      w[u] = ml[2 * (s + u)];
+      const float* src = a + static_cast<int64_t>(s + u) * D;
+      if constexpr (DPT == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(src);
+        x[u][0] = t.x;
+        x[u][1] = t.y;
+        x[u][2] = t.z;
+        x[u][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(src);
+        x[u][0] = t.x;
+        x[u][1] = t.y;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float wu = fast_exp2(w[u] - M);
+#pragma unroll
+      for (int k = 0; k < DPT; ++k) acc[k] = fmaf(wu, x[u][k], acc[k]);
+    }
+  }
+  for (; s < nsplit; ++s) {
+    const float wu = fast_exp2(ml[2 * s] - M);
+#pragma unroll
+    for (int k = 0; k < DPT; ++k) acc[k] = fmaf(wu, a[static_cast<int64_t>(s) * D + k], acc[k]);
   }
   OutT* o = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + h * p.o_sh + lane * DPT;
 #pragma unroll
