@@ -169,6 +169,42 @@ FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tenso
                               void *workspace, size_t workspace_bytes, int split_tokens,
                               void *stream);
 
+/*
+ * forge_paged_gqa_decode_noalloc -- forge_paged_gqa_decode for callers that
+ * must not allocate device memory.  (The pages have no counterpart: this is
+ * an entry point of this library only.)
+ *
+ * Who needs it: code that decodes while a stream is being captured into a
+ * CUDA graph, where cudaMalloc (not a stream operation, and synchronising) is
+ * not allowed, and processes that fix their device memory at start-up -- a
+ * serving loop that gave everything else to its KV pool -- and must not
+ * allocate later.  forge_paged_gqa_decode may cudaMalloc its split scratch on
+ * first use; this call never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ * Arguments, layouts, results and errors are those of forge_paged_gqa_decode.
+ * The split scratch is a static device array of FORGE_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  The call uses the automatic split length if its
+ * scratch fits there, else 1024-token splits; if even those need more, it
+ * returns FORGE_ERR_WORKSPACE before enqueuing anything.  (At 32 query
+ * heads and D 128, 16 MiB covers batch 32 with block tables of up to 16K
+ * tokens; it needs about B * Hq * ceil(table tokens / split) * (D + 2) * 4
+ * bytes.)
+ *
+ * The first call on a device looks up the array's device address (a
+ * cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the one
+ * array and leaves its contents behind; nothing in it needs clearing, since
+ * each call writes every scratch value it reads.  Calls that overlap on the
+ * GPU (other streams, other threads) race on the array: serialise them.
+ */
+#define FORGE_NOALLOC_SCRATCH_BYTES (16u << 20)
+FORGE_API int forge_paged_gqa_decode_noalloc(const forge_tensor *q, const forge_tensor *k_cache,
+                                   const forge_tensor *v_cache, const forge_tensor *block_tables,
+                                   const forge_tensor *context_lens, float scale, forge_tensor *out,
+                                   void *stream);
+
 /* Human-readable name of a forge_status.  Never NULL. */
 FORGE_API const char *forge_status_string(int status);
 

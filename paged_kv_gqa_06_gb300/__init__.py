@@ -20,6 +20,7 @@ __all__ = [
     "forge_paged_kv_append",
     "forge_paged_gqa_decode",
     "forge_paged_gqa_decode_ex",
+    "forge_paged_gqa_decode_noalloc",
     "forge_paged_gqa_decode_workspace_bytes",
     "forge_paged_get_device_error",
 ]

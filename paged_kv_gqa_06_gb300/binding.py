@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_paged_gqa_decode_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, P, ctypes.c_size_t,
                                                   ctypes.c_int, P]
         lib.forge_paged_gqa_decode_ex.restype = ctypes.c_int
+        lib.forge_paged_gqa_decode_noalloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, P]
+        lib.forge_paged_gqa_decode_noalloc.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
         lib.forge_paged_gqa_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.forge_status_string.argtypes = [ctypes.c_int]
@@ -126,6 +128,17 @@ def forge_paged_gqa_decode(q, k_cache, v_cache, block_tables, context_lens, scal
                                     _ref(describe(block_tables)), _ref(describe(context_lens)),
                                     float(scale), _ref(describe(out)), _stream_ptr(stream))
     _raise(rc, "forge_paged_gqa_decode")
+    return out
+
+
+def forge_paged_gqa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):
+    """Decode for callers that cannot allocate device memory: the split scratch
+    is a static array inside the library (see include/forge_paged.h)."""
+    lib = load_library()
+    rc = lib.forge_paged_gqa_decode_noalloc(_ref(describe(q)), _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                            _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                            float(scale), _ref(describe(out)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_gqa_decode_noalloc")
     return out
 
 
