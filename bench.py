@@ -284,16 +284,12 @@ def run_native(args, wl, out_bytes):
 
     stream = torch.cuda.Stream(device=dev)
     bytes_step = wl.bytes_decode(out_bytes)
-    launches_per_step = 1 + 1 + (1 if wl.MB * 16 > 512 else 0)
+    launches_per_step = 2  # append + decode (the split merge runs inside the decode kernel)
 
-    def step(ev_a=None, ev_b=None):
+    def step():
         binding.forge_paged_kv_append(d["k_new"], d["v_new"], d["slots"], k_cache, v_cache, stream=stream)
-        if ev_a is not None:
-            ev_a.record(stream)
         binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale, out,
                                        stream=stream)
-        if ev_b is not None:
-            ev_b.record(stream)
 
     def e2e_step():
         for k in ("q", "k_new", "v_new", "slots", "tables", "lens"):
@@ -302,14 +298,41 @@ def run_native(args, wl, out_bytes):
         host_out.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
+        for _ in range(3):
+            step()  # eager calls first: the decode sizes its workspace on this stream
     stream.synchronize()
     assert binding.forge_paged_get_device_error(stream) == 0
 
+    # The timed loop replays CUDA graphs that each hold `chunk` whole steps
+    # (append + decode), the way a serving loop replays a captured decode
+    # step: no Python or per-call launch overhead between kernels.  With
+    # --no-graphs the loop makes eager C-ABI calls instead.
+    chunk = max(c for c in range(1, 21) if args.steps % c == 0) if args.graphs else 1
+    g_steps = g_dec = None
+    if args.graphs:
+        g_steps, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g_steps, stream=stream):
+                for _ in range(chunk):
+                    step()
+            with torch.cuda.graph(g_dec, stream=stream):
+                for _ in range(chunk):
+                    binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale,
+                                                   out, stream=stream)
+    reps = args.steps // chunk
+
+    def run_chunk():
+        if g_steps is not None:
+            g_steps.replay()
+        else:
+            step()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup) // chunk + 1):
+            run_chunk()
+    stream.synchronize()
+
     # ---------------- timed region (device-resident inputs)
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(_gpu_id(torch, dev.index or 0)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -319,17 +342,31 @@ def run_native(args, wl, out_bytes):
     w0 = time.time()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for k in range(args.steps):
-            step(ev_a[k], ev_b[k])
+        for _ in range(reps):
+            run_chunk()
         end.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
     if ws > 1:
         dist.barrier()
     ms_total = start.elapsed_time(end)
-    decode_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
     rows = sampler.stop() if sampler else []
     clocks = ClockSampler.summarize(rows, w0, w1) if sampler else None
+
+    # ---------------- the decode kernel alone, same launch path, events on its stream
+    dec_reps = max(1, min(reps, 2000 // chunk))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(dec_reps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for r in range(dec_reps):
+            if g_dec is not None:
+                g_dec.replay()
+            else:
+                binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale, out,
+                                               stream=stream)
+            ev[r + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    decode_ms = [ev[r].elapsed_time(ev[r + 1]) / chunk for r in range(dec_reps)]
 
     # ---------------- end to end: host buffers, copies inside the timed region
     e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -372,12 +409,14 @@ def run_native(args, wl, out_bytes):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_layer_step": round(ms_step * 1e3, 2),
         "pct_of_hbm_peak": round(100.0 * value / ws / peak, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
-        "config": _config_dict(wl, {"l2": "no flush: inputs larger than L2 (KV pool "
+        "config": _config_dict(wl, {"launch": (f"CUDA graphs of {chunk} steps (append + decode) replayed"
+                                               if args.graphs else "eager C-ABI calls"),
+                                    "l2": "no flush: inputs larger than L2 (KV pool "
                                           f"{2 * k_cache.numel() * 2 / 1e6:.0f} MB vs 126 MB L2)",
                                     "bytes_per_step": bytes_step,
                                     "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_gqa_decode_split_kernel, timed with its split reduce (one decode call)",
+                     "kernel": "paged_gqa_decode_split_kernel (one decode call; split merge inside)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),
@@ -401,6 +440,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="qwen3_4b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", dest="graphs", action="store_false",
+                    help="time eager C-ABI calls instead of replaying captured steps")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -133,12 +133,12 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  *
  * Supported: D in {64, 128}; BS = 16; G = Hq/Hkv in {1, 2, 4, 8}.
  * Work is split along the context in splits of up to 512 tokens (fewer for
- * short tables); sequences with more than one split are merged by a second
- * kernel.  The split scratch is a per-(device, stream) buffer that the
- * library allocates with cudaMalloc on first need and keeps, growing it when
- * a larger problem arrives; the first call of a given size on a stream
- * should therefore come before any stream capture.  Use
- * forge_paged_gqa_decode_ex to pass caller-owned scratch instead.
+ * short tables); for a sequence with more than one split, the last split to
+ * finish merges them.  The split scratch is a per-(device, stream) buffer
+ * that the library allocates with cudaMalloc (and zero-fills) on first need
+ * and keeps, growing it when a larger problem arrives; the first call of a
+ * given size on a stream should therefore come before any stream capture.
+ * Use forge_paged_gqa_decode_ex to pass caller-owned scratch instead.
  * Thread-safe.
  */
 FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *k_cache,
@@ -148,9 +148,10 @@ FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *
 
 /*
  * Bytes of split scratch that forge_paged_gqa_decode_ex needs for these
- * sizes and split length.  split_tokens = 0 picks the same split length as
- * forge_paged_gqa_decode; otherwise it must be a multiple of 16 in
- * [16, 1024].  Returns 0 for invalid sizes.  Host-only, no CUDA call.
+ * sizes and split length (split_tokens a multiple of 16 in [16, 1024]).
+ * split_tokens = 0 returns an upper bound valid for the automatic split
+ * length.  Returns 0 when no scratch is needed (one split per sequence) or
+ * the sizes are invalid.  Host-only, no CUDA call.
  */
 FORGE_API size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
                                               int max_blocks_per_seq, int split_tokens);
@@ -160,8 +161,13 @@ FORGE_API size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, 
  * scratch (device memory, 256-byte aligned, at least
  * forge_paged_gqa_decode_workspace_bytes(...) bytes; may be NULL only when
  * that size is 0) and an explicit split length in tokens (0 = automatic,
- * else a multiple of 16 in [16, 1024]).  Allocates nothing.  Calls that
- * share one workspace must not overlap on the GPU.
+ * else a multiple of 16 in [16, 1024]).  Allocates nothing.  The first 256
+ * KiB of a workspace hold split arrival counters (one per sequence and KV
+ * head, so B * Hkv <= 65536 whenever scratch is needed): zero-fill the
+ * workspace once before its first use; every completed call leaves the
+ * counters at zero and writes nothing else there, so one workspace may then
+ * serve calls of any shape without clearing.  Calls that share one workspace
+ * must not overlap on the GPU.
  */
 FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tensor *k_cache,
                               const forge_tensor *v_cache, const forge_tensor *block_tables,
@@ -195,8 +201,10 @@ FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tenso
  * The first call on a device looks up the array's device address (a
  * cudaGetSymbolAddress, with that device current) and caches it; make that
  * first call before any stream capture.  Every call on a device shares the one
- * array and leaves its contents behind; nothing in it needs clearing, since
- * each call writes every scratch value it reads.  Calls that overlap on the
+ * array and leaves its contents behind.  The only part that must start at
+ * zero, the split arrival counters, is zero when the library loads (static
+ * device memory) and every completed call returns it to zero; all other
+ * scratch values are written before they are read.  Calls that overlap on the
  * GPU (other streams, other threads) race on the array: serialise them.
  */
 #define FORGE_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -79,12 +79,27 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         return lib
 
 
+_desc_cache: dict = {}
+_DESC_CACHE_MAX = 4096
+
+
 def describe(t: torch.Tensor | None) -> ForgeTensor | None:
-    """forge_tensor descriptor of a torch tensor (no copy)."""
+    """forge_tensor descriptor of a torch tensor (no copy).
+
+    Descriptors are cached by (address, dtype, shape, strides): a decode loop
+    passes the same tensors every step, and filling a ctypes struct costs
+    more host time than the lookup.  The C side only reads them.
+    """
     if t is None:
         return None
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _desc_cache.get(key)
+    if d is not None:
+        return d
     if t.dim() > 4:
         raise ValueError("forge tensors have at most 4 dims")
+    if len(_desc_cache) >= _DESC_CACHE_MAX:
+        _desc_cache.clear()
     d = ForgeTensor()
     d.data = t.data_ptr() if t.numel() > 0 else 0
     d.dtype = _DTYPES.get(t.dtype, 0)
@@ -92,6 +107,7 @@ def describe(t: torch.Tensor | None) -> ForgeTensor | None:
     for i in range(t.dim()):
         d.shape[i] = t.shape[i]
         d.stride[i] = t.stride(i)
+    _desc_cache[key] = d
     return d
 
 

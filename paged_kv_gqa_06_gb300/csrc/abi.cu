@@ -10,6 +10,8 @@
 #include <mutex>
 #include <utility>
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "../../include/forge_paged.h"
 #include "common.cuh"
 
@@ -104,7 +106,46 @@ struct DecodePlan {
   int D, G;
   bool out_bf16;
   size_t ws_bytes;
+  const forge_tensor* k_cache;
+  const forge_tensor* v_cache;
 };
+
+// cuTensorMapEncodeTiled from the driver, looked up through the runtime so
+// that the library does not link libcuda.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Tensor map over a [NB, Hkv, 16, D] bf16 cache, dims listed innermost first
+// (D, token, head, block), boxes of 64 dims x 16 tokens (128-byte rows) with
+// the 128-byte swizzle the decode kernel's shared-memory addressing expects.
+int encode_cache_map(const forge_tensor* c, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return FORGE_ERR_CUDA;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(c->shape[3]), static_cast<cuuint64_t>(kBlockSize),
+                              static_cast<cuuint64_t>(c->shape[1]),
+                              static_cast<cuuint64_t>(c->shape[0] > 0 ? c->shape[0] : 1)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c->stride[2]) * 2, static_cast<cuuint64_t>(c->stride[1]) * 2,
+                                 static_cast<cuuint64_t>(c->stride[0]) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockSize), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  void* base = c->data;
+  static unsigned char dummy[16] __attribute__((aligned(16)));
+  if (!base) base = dummy;  // empty pool: the map is never used
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_UNSUPPORTED;
+}
 
 int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms) {
   if (split_tokens > 0) return split_tokens / kBlockSize;
@@ -121,18 +162,29 @@ int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms) {
   return bps;
 }
 
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Split workspace: a fixed prefix of kCounterSlots int32 arrival counters
+// (one per (sequence, KV head), so B * Hkv <= kCounterSlots) | [B*Hq, s_max,
+// D] fp32 accumulators | [B*Hq, s_max, 2] fp32 (max, sum).  The prefix has
+// the same size for every shape, so no call's data ever lands on counters:
+// once zeroed, the counters stay zero between calls (each call returns the
+// ones it used to zero), whatever shapes share the workspace.
+constexpr int64_t kCounterSlots = 65536;
+constexpr size_t kCounterBytes = kCounterSlots * 4;
+
 size_t workspace_bytes_for(int64_t B, int64_t Hq, int64_t D, int64_t s_max) {
   if (s_max <= 1) return 0;
   const size_t acc = static_cast<size_t>(B * Hq * s_max * D) * 4;
   const size_t ml = static_cast<size_t>(B * Hq * s_max * 2) * 4;
-  return ((acc + 255) & ~static_cast<size_t>(255)) + ml;
+  return kCounterBytes + round256(acc) + ml;
 }
 
 int nstage_default() {
   static int v = [] {
     const char* e = std::getenv("FORGE_PAGED_NSTAGE");
     int n = e ? std::atoi(e) : 0;
-    return (n >= 2 && n <= 16) ? n : 4;
+    return (n >= 2 && n <= 16) ? n : 2;
   }();
   return v;
 }
@@ -168,6 +220,8 @@ int plan_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_
     return FORGE_ERR_VALUE;
 
   std::memset(plan, 0, sizeof(*plan));
+  plan->k_cache = k_cache;
+  plan->v_cache = v_cache;
   plan->D = static_cast<int>(D);
   plan->G = static_cast<int>(G);
   plan->out_bf16 = out->dtype == FORGE_BF16;
@@ -202,26 +256,34 @@ int plan_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_
   p.MB = static_cast<int>(MB);
   p.bps = split_blocks_for(split_tokens, p.B, p.Hkv, p.MB, num_sms);
   p.s_max = MB > 0 ? static_cast<int>((MB + p.bps - 1) / p.bps) : 1;
+  if (p.s_max > 65535) return FORGE_ERR_UNSUPPORTED;  // grid z limit
   p.nstage = nstage_default();
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   plan->ws_bytes = workspace_bytes_for(B, Hq, D, p.s_max);
+  if (plan->ws_bytes > 0 && B * Hkv > kCounterSlots) return FORGE_ERR_UNSUPPORTED;
   return FORGE_OK;
 }
 
 void attach_workspace(DecodePlan* plan, void* ws) {
   forge::DecodeParams& p = plan->p;
   if (plan->ws_bytes == 0) {
+    p.counters = nullptr;
     p.ws_acc = nullptr;
     p.ws_ml = nullptr;
     return;
   }
-  const size_t acc = static_cast<size_t>(p.B) * p.Hq * p.s_max * plan->D * 4;
-  p.ws_acc = static_cast<float*>(ws);
-  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((acc + 255) & ~static_cast<size_t>(255)));
+  char* base = static_cast<char*>(ws);
+  const size_t acc = round256(static_cast<size_t>(p.B) * p.Hq * p.s_max * plan->D * 4);
+  p.counters = reinterpret_cast<int*>(base);
+  p.ws_acc = reinterpret_cast<float*>(base + kCounterBytes);
+  p.ws_ml = reinterpret_cast<float*>(base + kCounterBytes + acc);
 }
 
 int launch_plan(DecodePlan* plan, cudaStream_t stream) {
-  if (forge::launch_decode(plan->p, plan->D, plan->G, plan->out_bf16, stream) != cudaSuccess)
+  CUtensorMap tmk, tmv;
+  FORGE_TRY(encode_cache_map(plan->k_cache, &tmk));
+  FORGE_TRY(encode_cache_map(plan->v_cache, &tmv));
+  if (forge::launch_decode(plan->p, tmk, tmv, plan->D, plan->G, plan->out_bf16, stream) != cudaSuccess)
     return FORGE_ERR_CUDA;
   return FORGE_OK;
 }
@@ -239,6 +301,11 @@ int cached_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
     }
     void* p = nullptr;
     if (cudaMalloc(&p, bytes) != cudaSuccess) return FORGE_ERR_CUDA;
+    // the split arrival counters start at zero (kernels return them to zero)
+    if (cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) {
+      cudaFree(p);
+      return FORGE_ERR_CUDA;
+    }
     slot = {p, bytes};
   }
   *out = slot.first;

@@ -6,6 +6,7 @@
 // the C ABI layer fills in.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the library does not link libcuda)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -48,6 +49,7 @@ struct DecodeParams {
   const int32_t* context_lens;
   void* out;
   int64_t o_sb, o_sh;
+  int* counters;   // [B*Hkv] split arrivals per (sequence, KV head); zero between calls
   float* ws_acc;   // [B*Hq, s_max, D] unnormalised split accumulators
   float* ws_ml;    // [B*Hq, s_max, 2] split (max, sum) in log2 units
   int B, Hq, Hkv, NB, MB;
@@ -129,6 +131,49 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// One tiled box of a 4-D tensor map (TMA engine) into shared memory,
+// completing its bytes on `bar`.  c0 is the innermost coordinate; c0 times
+// the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four 8x8 b16 matrices from shared memory; lanes 8i..8i+7 give the row
+// addresses of matrix i, register i receives it (row lane/4, cols 2(lane%4)+{0,1}).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// As ldsm_x4, each matrix transposed (register i holds rows 2(lane%4)+{0,1}, col lane/4).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// d += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate, one warp.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Barrier among the first `nthreads` threads of the CTA (named barrier `id`).
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -162,7 +207,8 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 // Launchers (defined in append.cu / decode.cu).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, int D, int G, bool out_bf16, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int D, int G,
+                          bool out_bf16, cudaStream_t stream);
 size_t decode_smem_bytes(int D, int G, int bps, int nstage);
 
 }  // namespace forge

@@ -8,29 +8,32 @@
 //   out[b,h,:] = sum_{t<L} softmax_t(scale * q[b,h,:] . K[t, h/G, :]) V[t, h/G, :]
 // where token t lives in physical block block_tables[b][t/16], slot t%16.
 //
-// Work decomposition (HBM-bound: ~2 fp32 FMA per byte of K/V at G = 4):
-//   * one CTA per (split, KV head g, sequence b).  A split is a run of up to
-//     `bps` consecutive KV blocks of one sequence; every K/V byte is read once
-//     and used for all G query heads of its group;
-//   * warp 4 is the producer: it translates logical blocks through the block
+// Work decomposition.  The path is HBM-bound (each K/V byte is used for G
+// query heads); the kernel's job is to stream every byte once with as few
+// SM instructions per byte as possible:
+//   * one CTA per (KV head g, sequence b, split).  A split is a run of up to
+//     `bps` consecutive KV blocks of one sequence;
+//   * warp 2 is the producer: it translates logical blocks through the block
 //     table and streams the split's K tiles, then its V tiles, into a ring of
-//     shared-memory stages.  A stage holds two (block, head) tiles (16 x D
-//     bf16 each, one contiguous run apiece), moved by single bulk copies on
-//     the TMA engine and tracked by one mbarrier;
-//   * warps 0-3 consume: 8 lanes per token, D/8 dims per lane, two tokens
-//     per thread per stage.  Pass 1 forms the G logits of every token of the
-//     split (packed fp32x2 FMA on bf16 widened exactly) and sums each 8-lane
-//     group with a transposing shuffle reduction that ends with one (token,
-//     head) logit per lane; the split's max and sum are then taken over all
-//     logits at once (no running rescale); pass 2 accumulates p * V in
-//     registers;
-//   * a split that is the whole sequence writes `out` directly; otherwise it
-//     writes unnormalised (acc, max, sum) and the reduce kernel merges the
-//     splits of each (b, h).
-// Logits are kept in log2 units (q is prescaled by scale*log2 e) so that the
-// exponentials are single ex2 instructions.  Slots at t >= L are never
-// multiplied in: their logits are -inf and their V rows are skipped, so NaN
-// in unused slots cannot leak into the output.
+//     shared-memory stages with tiled TMA copies (tensor maps over the cache,
+//     128-byte swizzle).  A stage holds two (block, head) tiles of 16 x D
+//     bf16 and is tracked by one mbarrier;
+//   * warps 0 and 1 consume one tile each per stage on the tensor cores
+//     (mma.sync m16n8k16, bf16 in, fp32 accumulate; the G <= 8 query heads
+//     fill the n = 8 side).  Pass 1: logits S^T = K q^T, 16 tokens per tile,
+//     into shared memory in log2 units.  The split's max and sum are taken
+//     over all its logits at once (no running rescale).  Pass 2:
+//     O^T += V^T P^T with P split into bf16 high and low parts (two MMAs), so
+//     the weights keep ~16 bits of precision;
+//   * a split that is the whole sequence writes `out` directly.  Otherwise
+//     it writes unnormalised (acc, max, sum) to the workspace and counts
+//     itself in at a per-(b, g) arrival counter; the CTA that arrives last
+//     merges the splits of the G heads (the split reduce) and returns the
+//     counter to zero.  Merging in the last CTA, rather than in a second
+//     kernel, keeps the merge off the launch critical path.
+// Slots at t >= L never reach the output: their logits are -inf and their V
+// rows are zeroed in shared memory before the PV product, so NaN in unused
+// slots cannot leak in.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -40,29 +43,31 @@
 namespace forge {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kStageBlocks = 2;              // KV blocks (tiles) per pipeline stage
+constexpr int kConsumerWarps = kStageBlocks; // one tile per consumer warp per stage
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStageBlocks = 2;            // KV blocks per pipeline stage
-constexpr int kGroups = kConsumers / 8;    // token groups (8 lanes each)
+constexpr int kThreads = kConsumers + 32;    // + one producer warp
+constexpr int kBoxDims = 64;                 // dims per TMA box: 128 bytes, one swizzle span
+constexpr int kBoxBytes = kBlockSize * kBoxDims * 2;  // 2 KiB: 16 rows of 128 B
 
 struct SmemLayout {
   size_t ring, logits, red_ml, bars, total;
+  int lrow;  // logits row length (tokens) per head
 };
 
-// ring: nstage stages of kStageBlocks tiles; reused at the end for the
-// cross-group sum, [kGroups][G][D] fp32.  logits: [bps*16][G] fp32 (rounded
-// up to whole stages).
+// ring (1024-byte aligned for the 128-byte swizzle; reused at the end for the
+// consumer-warp merge [kConsumerWarps][G][D] fp32) | logits [G][lrow] fp32 |
+// per-warp (max, sum) | mbarriers.
 __host__ __device__ inline SmemLayout decode_layout(int D, int G, int bps, int nstage) {
   SmemLayout l;
-  size_t off = 0;
+  size_t off = 1024;  // room to round the ring up to a 1024-byte boundary
   l.ring = off;
   const size_t ring = static_cast<size_t>(nstage) * kStageBlocks * kBlockSize * D * 2;
-  const size_t red = static_cast<size_t>(kGroups) * G * D * 4;
+  const size_t red = static_cast<size_t>(kConsumerWarps) * G * D * 4;
   off += ring > red ? ring : red;
   l.logits = off;
-  const int bps_up = (bps + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
-  off += static_cast<size_t>(bps_up) * kBlockSize * G * 4;
+  l.lrow = (bps + kStageBlocks - 1) / kStageBlocks * kStageBlocks * kBlockSize;
+  off += static_cast<size_t>(G) * l.lrow * 4;
   l.red_ml = off;
   off += static_cast<size_t>(2) * kConsumerWarps * G * 4;
   off = (off + 15) & ~static_cast<size_t>(15);
@@ -70,39 +75,6 @@ __host__ __device__ inline SmemLayout decode_layout(int D, int G, int bps, int n
   off += static_cast<size_t>(2) * nstage * 8;
   l.total = off;
   return l;
-}
-
-template <int G>
-__device__ __forceinline__ void load_row(const float* src, float (&v)[G]) {
-  if constexpr (G % 4 == 0) {
-#pragma unroll
-    for (int k = 0; k < G / 4; ++k) {
-      const float4 t = reinterpret_cast<const float4*>(src)[k];
-      v[4 * k] = t.x;
-      v[4 * k + 1] = t.y;
-      v[4 * k + 2] = t.z;
-      v[4 * k + 3] = t.w;
-    }
-  } else if constexpr (G == 2) {
-    const float2 t = *reinterpret_cast<const float2*>(src);
-    v[0] = t.x;
-    v[1] = t.y;
-  } else {
-    v[0] = *src;
-  }
-}
-
-template <int G>
-__device__ __forceinline__ void store_row(float* dst, const float (&v)[G]) {
-  if constexpr (G % 4 == 0) {
-#pragma unroll
-    for (int k = 0; k < G / 4; ++k)
-      reinterpret_cast<float4*>(dst)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  } else if constexpr (G == 2) {
-    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
-  } else {
-    *dst = v[0];
-  }
 }
 
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
@@ -120,57 +92,140 @@ __device__ __forceinline__ int checked_length(const DecodeParams& p, int b, bool
   return L;
 }
 
-// Sum each of a lane's CNT values over the 8 lanes of its token group (lanes
-// that differ in bits 0..2).  At each exchange step a lane keeps one half of
-// the values it still holds and hands the other half to its partner, so the
-// shuffle count halves per step.  Afterwards lane `sub` holds the group sums
-// of values [first, first + max(N/8, 1)), returned in v[0..].
-template <int CNT, int M>
-struct Group8Sum {
-  template <int N>
-  static __device__ __forceinline__ void run(float (&v)[N], int sub, int& first) {
-    const bool hi = (sub & M) != 0;
-    if constexpr (CNT > 1) {
-      constexpr int H = CNT / 2;
-#pragma unroll
-      for (int k = 0; k < H; ++k) {
-        const float keep = hi ? v[H + k] : v[k];
-        const float send = hi ? v[k] : v[H + k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, M);
-      }
-      if (hi) first += H;
-      if constexpr (M > 1) Group8Sum<H, M / 2>::run(v, sub, first);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
-      if constexpr (M > 1) Group8Sum<1, M / 2>::run(v, sub, first);
-    }
-  }
-};
+// Shared-memory address of 16-byte chunk `chunk` (of D/8) in row `row` of a
+// tile stored as D/64 swizzled boxes: box = chunk / 8, and within a box the
+// chunk index is XORed with the row index mod 8 (TMA 128-byte swizzle).
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * kBoxBytes + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
+}
 
-// Load one token row slice: chunk c (16 bytes) of this lane sits at element
-// c * 64 + sub * 8, so the 8 lanes of a token read 128 contiguous bytes per
-// chunk (no shared-memory bank conflicts).
-template <int D>
-__device__ __forceinline__ void load_row_slice(const __nv_bfloat16* row, int sub, uint32_t (&w)[D / 16]) {
+// Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
+// x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Split reduce for the G heads of (b, g): with M = max_s m_s and
+// w_s = 2^(m_s - M), out = sum_s w_s acc_s / sum_s w_s l_s over the nsplit
+// partials in the workspace.  Run by the kConsumers threads of the last CTA:
+// the max and the denominator are reduced cooperatively, the weights of a
+// chunk of up to `wcap` splits are staged in shared memory (`wbuf`,
+// [G][wcap]), and each thread accumulates 4 consecutive dims of outputs with
+// 8 partial rows in flight.  Workspace reads bypass L1 (other SMs wrote them).
+template <int D, int G, typename OutT>
+__device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int g, int nsplit, int tid, float* wbuf,
+                                             int wcap, float* red_m, float* red_l) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t row0 = static_cast<int64_t>(b) * p.Hq + g * G;  // first head of the group
+  float M[G], den[G];
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-    const uint4 x = *reinterpret_cast<const uint4*>(row + c * 64 + sub * 8);
-    w[4 * c] = x.x;
-    w[4 * c + 1] = x.y;
-    w[4 * c + 2] = x.z;
-    w[4 * c + 3] = x.w;
+  for (int i = 0; i < G; ++i) {
+    const float* ml = p.ws_ml + (row0 + i) * p.s_max * 2;
+    float mx = -INFINITY;
+    for (int s = tid; s < nsplit; s += kConsumers) mx = fmaxf(mx, __ldcg(ml + 2 * s));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red_m[warp * G + i] = mx;
+  }
+  named_barrier(1, kConsumers);
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    M[i] = red_m[i];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) M[i] = fmaxf(M[i], red_m[w * G + i]);
+    const float* ml = p.ws_ml + (row0 + i) * p.s_max * 2;
+    float dn = 0.f;
+    for (int s = tid; s < nsplit; s += kConsumers) dn += fast_exp2(__ldcg(ml + 2 * s) - M[i]) * __ldcg(ml + 2 * s + 1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dn += __shfl_xor_sync(0xffffffffu, dn, off);
+    if (lane == 0) red_l[warp * G + i] = dn;
+  }
+  named_barrier(1, kConsumers);
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    den[i] = red_l[i];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) den[i] += red_l[w * G + i];
+  }
+
+  constexpr int kOut = (G * D / 4 + kConsumers - 1) / kConsumers;  // float4 outputs per thread
+  constexpr int U = 8;
+  float4 num[kOut];
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) num[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nsplit; s0 += wcap) {
+    const int cnt = min(wcap, nsplit - s0);
+    for (int idx = tid; idx < G * cnt; idx += kConsumers) {
+      const int i = idx / cnt, sl = idx % cnt;
+      float Mi = M[0];
+#pragma unroll
+      for (int k = 1; k < G; ++k)
+        if (i == k) Mi = M[k];
+      wbuf[i * wcap + sl] = fast_exp2(__ldcg(p.ws_ml + ((row0 + i) * p.s_max + s0 + sl) * 2) - Mi);
+    }
+    named_barrier(1, kConsumers);
+#pragma unroll
+    for (int k = 0; k < kOut; ++k) {
+      const int o4 = (tid + k * kConsumers) * 4;
+      if (o4 < G * D) {
+        const int i = o4 / D, d = o4 % D;
+        const float* acc = p.ws_acc + ((row0 + i) * p.s_max + s0) * D + d;
+        const float* w = wbuf + i * wcap;
+        float4 n = num[k];
+        for (int sl = 0; sl < cnt; sl += U) {
+          float4 x[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            x[u] = sl + u < cnt ? __ldcg(reinterpret_cast<const float4*>(acc + static_cast<int64_t>(sl + u) * D))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float wu = sl + u < cnt ? w[sl + u] : 0.f;
+            n.x = fmaf(wu, x[u].x, n.x);
+            n.y = fmaf(wu, x[u].y, n.y);
+            n.z = fmaf(wu, x[u].z, n.z);
+            n.w = fmaf(wu, x[u].w, n.w);
+          }
+        }
+        num[k] = n;
+      }
+    }
+    named_barrier(1, kConsumers);  // wbuf is rewritten by the next chunk
+  }
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) {
+    const int o4 = (tid + k * kConsumers) * 4;
+    if (o4 < G * D) {
+      const int i = o4 / D, d = o4 % D;
+      float dn = den[0];
+#pragma unroll
+      for (int j = 1; j < G; ++j)
+        if (i == j) dn = den[j];
+      OutT* dst = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + (g * G + i) * p.o_sh + d;
+      store_out(dst + 0, num[k].x / dn);
+      store_out(dst + 1, num[k].y / dn);
+      store_out(dst + 2, num[k].z / dn);
+      store_out(dst + 3, num[k].w / dn);
+    }
   }
 }
 
 template <int D, int G, typename OutT>
-__global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_split_kernel(const DecodeParams p) {
-  constexpr int WPL = D / 16;  // bf16 pairs per lane per token row
-  constexpr int TILE = kBlockSize * D;
-  constexpr uint32_t kTileBytes = TILE * sizeof(__nv_bfloat16);
-  constexpr int NV = kStageBlocks * G;  // logits a thread forms per stage
-  static_assert(D % 64 == 0, "8 lanes x whole 16-byte chunks per token row");
+__global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                          const __grid_constant__ CUtensorMap tmv,
+                                                                          const DecodeParams p) {
+  constexpr int TILE_BYTES = kBlockSize * D * 2;
+  constexpr int BOXES = D / kBoxDims;
+  constexpr int KSTEPS = D / 16;  // 16-dim MMA steps (QK) = 16-dim m-tiles (PV)
+  static_assert(D % kBoxDims == 0 && G >= 1 && G <= 8, "shape not built");
 
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // grid (KV head, sequence, split): all first splits are dispatched before
+  // any second split, so each sequence's shorter last split comes late.
+  const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
@@ -189,19 +244,22 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
   if (s >= nsplit) return;
 
   const int blk0 = s * p.bps;
-  const int n = min(p.bps, nblk - blk0);                    // KV blocks in this split (>= 1)
-  const int nks = (n + kStageBlocks - 1) / kStageBlocks;    // stages per pass
+  const int n = min(p.bps, nblk - blk0);                  // KV blocks in this split (>= 1)
+  const int nks = (n + kStageBlocks - 1) / kStageBlocks;  // stages per pass
   const int nstage = p.nstage;
 
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout lay = decode_layout(D, G, p.bps, nstage);
-  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem + lay.ring);
-  float* red = reinterpret_cast<float*>(smem + lay.ring);  // reuses the ring at the end
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t ring_s = (sbase + static_cast<uint32_t>(lay.ring)) & ~1023u;  // shared-space address
+  unsigned char* ring = smem + (ring_s - sbase);
+  float* red = reinterpret_cast<float*>(ring);  // consumer-warp merge, after the last stage
   float* logits = reinterpret_cast<float*>(smem + lay.logits);
   float* red_m = reinterpret_cast<float*>(smem + lay.red_ml);
   float* red_l = red_m + kConsumerWarps * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + nstage;
+  const int lrow = lay.lrow;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nstage; ++i) {
@@ -220,8 +278,6 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
     const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
                      (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
     if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
-    const __nv_bfloat16* kbase = p.k_cache + g * p.kc_sh;
-    const __nv_bfloat16* vbase = p.v_cache + g * p.vc_sh;
     int slot = 0;
     uint32_t phase = 0;
     for (int i = 0; i < 2 * nks; ++i) {
@@ -230,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
       int pb[kStageBlocks];
 #pragma unroll
       for (int u = 0; u < kStageBlocks; ++u) {
-        const int j = j0 + u;  // <= 63 < 2 * 32
+        const int j = j0 + u;  // <= 64
         pb[u] = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
         if (j >= n) pb[u] = -1;  // past the split: no tile
       }
@@ -239,16 +295,17 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
         uint32_t bytes = 0;
 #pragma unroll
         for (int u = 0; u < kStageBlocks; ++u)
-          if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += kTileBytes;
+          if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += TILE_BYTES;
         if (bytes) {
           mbar_arrive_expect_tx(full + slot, bytes);
-          const __nv_bfloat16* base = is_v ? vbase : kbase;
-          const int64_t sblk = is_v ? p.vc_sblk : p.kc_sblk;
+          const CUtensorMap* map = is_v ? &tmv : &tmk;
 #pragma unroll
-          for (int u = 0; u < kStageBlocks; ++u)
-            if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB))
-              bulk_copy_g2s(ring + (slot * kStageBlocks + u) * TILE, base + static_cast<int64_t>(pb[u]) * sblk,
-                            kTileBytes, full + slot);
+          for (int u = 0; u < kStageBlocks; ++u) {
+            if (static_cast<unsigned>(pb[u]) >= static_cast<unsigned>(p.NB)) continue;
+            unsigned char* tile = ring + (slot * kStageBlocks + u) * TILE_BYTES;
+#pragma unroll
+            for (int c = 0; c < BOXES; ++c) tma_load_4d(tile + c * kBoxBytes, map, c * kBoxDims, 0, g, pb[u], full + slot);
+          }
         } else {
           mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
         }
@@ -263,67 +320,59 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
 
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;  // 0 .. kConsumers-1
-  const int tok = tid >> 3;     // token row within each tile of a stage
-  const int sub = tid & 7;
+  const int tq = lane >> 2;     // MMA group id: a token (QK) / a dim (PV) row, and the head of B
+  const int tr = lane & 3;      // MMA thread-in-group: a pair of columns
   const int t_base = blk0 * kBlockSize;
 
-  // q of the G heads of this group, prescaled into log2 units, as float pairs
-  // in this lane's dims {c*64 + sub*8 + e}.
-  float2 q2[G][WPL];
+  // B operand of the QK product, q^T (k = dim, n = head), for all KSTEPS:
+  // {q[tq][16ks + 2tr], +1} and {q[tq][16ks + 8 + 2tr], +1}; heads >= G are 0.
+  uint32_t qb[KSTEPS][2];
+  {
+    const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + tq) * p.q_sh;
 #pragma unroll
-  for (int i = 0; i < G; ++i) {
-    uint32_t w[WPL];
-    load_row_slice<D>(p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + i) * p.q_sh, sub, w);
-#pragma unroll
-    for (int k = 0; k < WPL; ++k) {
-      const float2 f = bf16x2_to_float2(w[k]);
-      q2[i][k] = make_float2(f.x * p.qk_scale_log2, f.y * p.qk_scale_log2);
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      qb[ks][0] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
+      qb[ks][1] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
     }
   }
 
   int slot = 0;
   uint32_t phase = 0;
 
-  // ---- pass 1: logits of every token of the split (log2 units)
+  // ---- pass 1: logits of every token of the split (log2 units), one tile per warp per stage
   for (int st = 0; st < nks; ++st) {
     mbar_wait(full + slot, phase, p.err);
-    float v[NV];
+    const int j = st * kStageBlocks + warp;  // block within the split
+    if (j < n) {
+      const uint32_t tile = ring_s + (slot * kStageBlocks + warp) * TILE_BYTES;
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // token row this lane addresses
+      const int acol = lane >> 4;                           // +0 / +1 chunk
 #pragma unroll
-    for (int u = 0; u < kStageBlocks; ++u) {
-      uint32_t kw[WPL];
-      load_row_slice<D>(ring + (slot * kStageBlocks + u) * TILE + tok * D, sub, kw);
-      if (u == kStageBlocks - 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty + slot);
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(swz(tile, arow, 2 * ks + acol), a);
+        if (ks & 1)
+          mma_16816_bf16(c1, a, qb[ks][0], qb[ks][1]);
+        else
+          mma_16816_bf16(c0, a, qb[ks][0], qb[ks][1]);
       }
-      float2 acc[G];
-#pragma unroll
-      for (int i = 0; i < G; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < WPL; ++k) {
-        const float2 kf = bf16x2_to_float2(kw[k]);
-#pragma unroll
-        for (int i = 0; i < G; ++i) acc[i] = ffma2(q2[i][k], kf, acc[i]);
+      // c[0..1]: token tq, heads 2tr, 2tr+1; c[2..3]: token tq+8
+      const int pos = t_base + j * kBlockSize;
+      const bool v0 = pos + tq < L, v1 = pos + tq + 8 < L;
+      const int h0 = 2 * tr, h1 = 2 * tr + 1;
+      float* lg = logits + j * kBlockSize;
+      if (h0 < G) {
+        lg[h0 * lrow + tq] = v0 ? (c0[0] + c1[0]) * p.qk_scale_log2 : -INFINITY;
+        lg[h0 * lrow + tq + 8] = v1 ? (c0[2] + c1[2]) * p.qk_scale_log2 : -INFINITY;
       }
-#pragma unroll
-      for (int i = 0; i < G; ++i) v[u * G + i] = acc[i].x + acc[i].y;
-    }
-    int first = 0;
-    Group8Sum<NV, 4>::run(v, sub, first);
-    constexpr int kOut = NV >= 8 ? NV / 8 : 1;
-    constexpr int kDup = NV >= 8 ? 1 : 8 / NV;  // lanes holding the same sum
-    if ((sub & (kDup - 1)) == 0) {
-#pragma unroll
-      for (int k = 0; k < kOut; ++k) {
-        const int idx = first + k;
-        const int u = idx / G, i = idx % G;
-        const int j = st * kStageBlocks + u;  // block within the split
-        if (j < n) {
-          const bool valid = t_base + j * kBlockSize + tok < L;
-          logits[(j * kBlockSize + tok) * G + i] = valid ? v[k] : -INFINITY;
-        }
+      if (h1 < G) {
+        lg[h1 * lrow + tq] = v0 ? (c0[1] + c1[1]) * p.qk_scale_log2 : -INFINITY;
+        lg[h1 * lrow + tq + 8] = v1 ? (c0[3] + c1[3]) * p.qk_scale_log2 : -INFINITY;
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + slot);
     if (++slot == nstage) {
       slot = 0;
       phase ^= 1u;
@@ -336,15 +385,9 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
   {
     float mx[G];
 #pragma unroll
-    for (int i = 0; i < G; ++i) mx[i] = -INFINITY;
-    for (int t = tid; t < ntok; t += kConsumers) {
-      float x[G];
-      load_row<G>(logits + t * G, x);
-#pragma unroll
-      for (int i = 0; i < G; ++i) mx[i] = fmaxf(mx[i], x[i]);
-    }
-#pragma unroll
     for (int i = 0; i < G; ++i) {
+      mx[i] = -INFINITY;
+      for (int t = tid; t < ntok; t += kConsumers) mx[i] = fmaxf(mx[i], logits[i * lrow + t]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
     }
@@ -353,98 +396,106 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
       for (int i = 0; i < G; ++i) red_m[warp * G + i] = mx[i];
     }
     named_barrier(1, kConsumers);
-    float m[G];
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-      m[i] = red_m[i];
+      float m = red_m[i];
 #pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) m[i] = fmaxf(m[i], red_m[w * G + i]);
-    }
-    float sum[G];
-#pragma unroll
-    for (int i = 0; i < G; ++i) sum[i] = 0.f;
-    for (int t = tid; t < ntok; t += kConsumers) {
-      float x[G];
-      load_row<G>(logits + t * G, x);
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        x[i] = fast_exp2(x[i] - m[i]);
-        sum[i] += x[i];
+      for (int w = 1; w < kConsumerWarps; ++w) m = fmaxf(m, red_m[w * G + i]);
+      float sum = 0.f;
+      for (int t = tid; t < ntok; t += kConsumers) {
+        const float e = fast_exp2(logits[i * lrow + t] - m);
+        logits[i * lrow + t] = e;
+        sum += e;
       }
-      store_row<G>(logits + t * G, x);
-    }
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], off);
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int i = 0; i < G; ++i) red_l[warp * G + i] = sum[i];
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) red_l[warp * G + i] = sum;
     }
     named_barrier(1, kConsumers);
   }
 
-  // ---- pass 2: acc += p * V over this thread's tokens
-  float2 acc[G][WPL];
+  // ---- pass 2: O^T (dims x heads) += V^T P^T, one tile per warp per stage
+  float o[KSTEPS][4];
 #pragma unroll
-  for (int i = 0; i < G; ++i)
-#pragma unroll
-    for (int k = 0; k < WPL; ++k) acc[i][k] = make_float2(0.f, 0.f);
+  for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
   for (int st = 0; st < nks; ++st) {
     mbar_wait(full + slot, phase, p.err);
-    uint32_t vw[kStageBlocks][WPL];
-#pragma unroll
-    for (int u = 0; u < kStageBlocks; ++u)
-      load_row_slice<D>(ring + (slot * kStageBlocks + u) * TILE + tok * D, sub, vw[u]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + slot);
-#pragma unroll
-    for (int u = 0; u < kStageBlocks; ++u) {
-      const int j = st * kStageBlocks + u;
-      if (j < n && t_base + j * kBlockSize + tok < L) {
-        float w[G];
-        load_row<G>(logits + (j * kBlockSize + tok) * G, w);
-#pragma unroll
-        for (int k = 0; k < WPL; ++k) {
-          const float2 vf = bf16x2_to_float2(vw[u][k]);
-#pragma unroll
-          for (int i = 0; i < G; ++i) acc[i][k] = ffma2(make_float2(w[i], w[i]), vf, acc[i][k]);
+    const int j = st * kStageBlocks + warp;
+    if (j < n) {
+      const uint32_t tile = ring_s + (slot * kStageBlocks + warp) * TILE_BYTES;
+      const int pos = t_base + j * kBlockSize;
+      const int live = L - pos;  // >= 1 tokens of this block are in the sequence
+      if (live < kBlockSize) {
+        // the sequence ends inside this block: zero the V rows past its end
+        // (they may hold anything, NaN included; P is 0 there but 0*NaN is NaN)
+        unsigned char* trow = ring + (slot * kStageBlocks + warp) * TILE_BYTES;
+        for (int idx = lane; idx < (kBlockSize - live) * BOXES * 8; idx += 32) {
+          const int r = live + idx / (BOXES * 8), rest = idx % (BOXES * 8);
+          *reinterpret_cast<uint4*>(trow + (rest >> 3) * kBoxBytes + r * 128 + (rest & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // before the TMA engine refills this stage
+        __syncwarp();
+      }
+      // B operand P^T (k = token, n = head): {p[tq][2tr], +1}, {p[tq][8 + 2tr], +1}
+      uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
+      if (tq < G) {
+        const float* pr = logits + tq * lrow + j * kBlockSize + 2 * tr;
+        const float2 pa = *reinterpret_cast<const float2*>(pr);
+        const float2 pc = *reinterpret_cast<const float2*>(pr + 8);
+        split_bf16x2(pa.x, pa.y, bh0, bl0);
+        split_bf16x2(pc.x, pc.y, bh1, bl1);
+      }
+      const int arow = (lane & 7) + (lane >> 4) * 8;  // token row this lane addresses
+      const int acol = (lane >> 3) & 1;               // +0 / +1 chunk
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(swz(tile, arow, 2 * mt + acol), a);
+        mma_16816_bf16(o[mt], a, bh0, bh1);
+        mma_16816_bf16(o[mt], a, bl0, bl1);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + slot);
     if (++slot == nstage) {
       slot = 0;
       phase ^= 1u;
     }
   }
 
-  // ---- combine the kGroups token groups through shared memory (the ring is
-  // free: every stage has been consumed by all consumer warps)
+  // ---- merge the consumer warps' partial O through shared memory (the ring
+  // is free: every stage has been consumed)
   named_barrier(1, kConsumers);
+  {
+    const int h0 = 2 * tr, h1 = 2 * tr + 1;
 #pragma unroll
-  for (int i = 0; i < G; ++i)
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      float4* dst = reinterpret_cast<float4*>(red + (tok * G + i) * D + c * 64 + sub * 8);
-      dst[0] = make_float4(acc[i][4 * c].x, acc[i][4 * c].y, acc[i][4 * c + 1].x, acc[i][4 * c + 1].y);
-      dst[1] = make_float4(acc[i][4 * c + 2].x, acc[i][4 * c + 2].y, acc[i][4 * c + 3].x, acc[i][4 * c + 3].y);
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      const int d0 = 16 * mt + tq, d1 = d0 + 8;
+      if (h0 < G) {
+        red[(warp * G + h0) * D + d0] = o[mt][0];
+        red[(warp * G + h0) * D + d1] = o[mt][2];
+      }
+      if (h1 < G) {
+        red[(warp * G + h1) * D + d0] = o[mt][1];
+        red[(warp * G + h1) * D + d1] = o[mt][3];
+      }
     }
+  }
   named_barrier(1, kConsumers);
 
-  for (int o = tid * 4; o < G * D; o += kConsumers * 4) {
-    const int i = o / D, d = o % D;
+  for (int o4 = tid * 4; o4 < G * D; o4 += kConsumers * 4) {
+    const int i = o4 / D, d = o4 % D;
     float4 t = *reinterpret_cast<const float4*>(red + i * D + d);
 #pragma unroll
-    for (int grp = 1; grp < kGroups; ++grp) {
-      const float4 x = *reinterpret_cast<const float4*>(red + (grp * G + i) * D + d);
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(red + (w * G + i) * D + d);
       t.x += x.x;
       t.y += x.y;
       t.z += x.z;
       t.w += x.w;
     }
-    // the split's sum for head i: total of the per-warp sums
     float li = red_l[i];
 #pragma unroll
     for (int w = 1; w < kConsumerWarps; ++w) li += red_l[w * G + i];
@@ -459,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
       *reinterpret_cast<float4*>(p.ws_acc + ((static_cast<int64_t>(b) * p.Hq + h) * p.s_max + s) * D + d) = t;
     }
   }
-  if (nsplit > 1 && tid < G) {
+  if (nsplit == 1) return;
+  if (tid < G) {
     float mi = red_m[tid], li = red_l[tid];
 #pragma unroll
     for (int w = 1; w < kConsumerWarps; ++w) {
@@ -470,74 +522,17 @@ __global__ void __launch_bounds__(kThreads, (G >= 8 ? 1 : 4)) paged_gqa_decode_s
     p.ws_ml[2 * r] = mi;
     p.ws_ml[2 * r + 1] = li;
   }
-}
 
-// Merge the split partials of every (b, h) whose sequence has more than one
-// split: with M = max_s m_s and w_s = 2^(m_s - M),
-//   out = sum_s w_s acc_s / sum_s w_s l_s.
-// One warp per (b, h); each lane owns D/32 consecutive dims.  The split loop
-// is unrolled by 8 so that eight partial rows are in flight at once.
-template <int D, typename OutT>
-__global__ void __launch_bounds__(128) paged_gqa_decode_reduce_kernel(const DecodeParams p) {
-  constexpr int DPT = D / 32;
-  constexpr int U = 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rowid = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (rowid >= static_cast<int64_t>(p.B) * p.Hq) return;
-  const int b = static_cast<int>(rowid / p.Hq), h = static_cast<int>(rowid % p.Hq);
-  const int L = checked_length(p, b, false);
-  const int nblk = (L + kBlockSize - 1) / kBlockSize;
-  const int nsplit = (nblk + p.bps - 1) / p.bps;
-  if (nsplit <= 1) return;
-
-  const float* ml = p.ws_ml + rowid * p.s_max * 2;
-  float M = -INFINITY;
-  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float lsum = 0.f;
-  for (int s = lane; s < nsplit; s += 32) lsum += fast_exp2(ml[2 * s] - M) * ml[2 * s + 1];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-
-  float acc[DPT];
-#pragma unroll
-  for (int k = 0; k < DPT; ++k) acc[k] = 0.f;
-  const float* a = p.ws_acc + rowid * p.s_max * D + lane * DPT;
-  int s = 0;
-  for (; s + U <= nsplit; s += U) {
-    float x[U][DPT], w[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      w[u] = ml[2 * (s + u)];
-      const float* src = a + static_cast<int64_t>(s + u) * D;
-      if constexpr (DPT == 4) {
-        const float4 t = *reinterpret_cast<const float4*>(src);
-        x[u][0] = t.x;
-        x[u][1] = t.y;
-        x[u][2] = t.z;
-        x[u][3] = t.w;
-      } else {
-        const float2 t = *reinterpret_cast<const float2*>(src);
-        x[u][0] = t.x;
-        x[u][1] = t.y;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float wu = fast_exp2(w[u] - M);
-#pragma unroll
-      for (int k = 0; k < DPT; ++k) acc[k] = fmaf(wu, x[u][k], acc[k]);
-    }
-  }
-  for (; s < nsplit; ++s) {
-    const float wu = fast_exp2(ml[2 * s] - M);
-#pragma unroll
-    for (int k = 0; k < DPT; ++k) acc[k] = fmaf(wu, a[static_cast<int64_t>(s) * D + k], acc[k]);
-  }
-  OutT* o = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + h * p.o_sh + lane * DPT;
-#pragma unroll
-  for (int k = 0; k < DPT; ++k) store_out(o + k, acc[k] / lsum);
+  // ---- split reduce by the last CTA of (b, g) to arrive
+  __threadfence();  // this thread's partial stores, device-wide, before the arrival
+  named_barrier(1, kConsumers);
+  int* counter = p.counters + static_cast<int64_t>(b) * p.Hkv + g;
+  if (tid == 0) red_m[0] = __int_as_float(atomicAdd(counter, 1) == nsplit - 1 ? 1 : 0);
+  named_barrier(1, kConsumers);
+  if (__float_as_int(red_m[0]) == 0) return;
+  __threadfence();  // every other split's partial is now visible; read it past L1
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, logits, lrow, red_m, red_l);
+  if (tid == 0) *counter = 0;  // ready for the next call
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device and size.
@@ -560,28 +555,26 @@ cudaError_t ensure_smem(K kernel, size_t bytes, std::atomic<size_t> (&set_for)[6
 }
 
 template <int D, int G, typename OutT>
-cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_typed(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                         cudaStream_t stream) {
   const size_t smem = decode_layout(D, G, p.bps, p.nstage).total;
   auto split_kernel = paged_gqa_decode_split_kernel<D, G, OutT>;
   static std::atomic<size_t> smem_set[64];  // one record per instantiation
   cudaError_t e = ensure_smem(split_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(p.s_max), static_cast<unsigned>(p.Hkv), static_cast<unsigned>(p.B));
-  split_kernel<<<grid, kThreads, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.s_max <= 1) return e;
-  const int64_t rows = static_cast<int64_t>(p.B) * p.Hq;
-  paged_gqa_decode_reduce_kernel<D, OutT><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+  const dim3 grid(static_cast<unsigned>(p.Hkv), static_cast<unsigned>(p.B), static_cast<unsigned>(p.s_max));
+  split_kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
   return cudaGetLastError();
 }
 
 template <int D, typename OutT>
-cudaError_t launch_g(const DecodeParams& p, int G, cudaStream_t stream) {
+cudaError_t launch_g(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int G,
+                     cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_typed<D, 1, OutT>(p, stream);
-    case 2: return launch_typed<D, 2, OutT>(p, stream);
-    case 4: return launch_typed<D, 4, OutT>(p, stream);
-    case 8: return launch_typed<D, 8, OutT>(p, stream);
+    case 1: return launch_typed<D, 1, OutT>(p, tmk, tmv, stream);
+    case 2: return launch_typed<D, 2, OutT>(p, tmk, tmv, stream);
+    case 4: return launch_typed<D, 4, OutT>(p, tmk, tmv, stream);
+    case 8: return launch_typed<D, 8, OutT>(p, tmk, tmv, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -592,13 +585,16 @@ size_t decode_smem_bytes(int D, int G, int bps, int nstage) {
   return decode_layout(D, G, bps, nstage).total;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int D, int G, bool out_bf16, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int D, int G,
+                          bool out_bf16, cudaStream_t stream) {
   if (p.B == 0) return cudaSuccess;
   if (D == 128) {
-    return out_bf16 ? launch_g<128, __nv_bfloat16>(p, G, stream) : launch_g<128, float>(p, G, stream);
+    return out_bf16 ? launch_g<128, __nv_bfloat16>(p, tmk, tmv, G, stream)
+                    : launch_g<128, float>(p, tmk, tmv, G, stream);
   }
   if (D == 64) {
-    return out_bf16 ? launch_g<64, __nv_bfloat16>(p, G, stream) : launch_g<64, float>(p, G, stream);
+    return out_bf16 ? launch_g<64, __nv_bfloat16>(p, tmk, tmv, G, stream)
+                    : launch_g<64, float>(p, tmk, tmv, G, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -23,8 +23,10 @@ constexpr int kMaxDevices = 64;
 constexpr int kFallbackSplitTokens = 1024;  // largest split: smallest scratch
 
 // Split scratch shared by every call of forge_paged_gqa_decode_noalloc on a
-// device.  It is never cleared: every value the decode reads from it is
-// written earlier in the same call.
+// device.  It is never cleared by this file: its split arrival counters are
+// zero at load (static device memory is zero-initialised) and every completed
+// decode returns them to zero, and every other value the decode reads from
+// it is written earlier in the same call.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;

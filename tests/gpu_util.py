@@ -47,7 +47,7 @@ class DeviceLayer:
                                                   self.wl.scale, out)
         nbytes = binding.forge_paged_gqa_decode_workspace_bytes(self.wl.B, self.wl.Hq, self.wl.Hkv, self.wl.D,
                                                                 self.wl.MB, split_tokens)
-        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=DEV)
         return binding.forge_paged_gqa_decode_ex(self.q, self.k_cache, self.v_cache, self.tables, self.lens,
                                                  self.wl.scale, out, ws, split_tokens)
 

@@ -42,7 +42,8 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_bytes_is_host_only(lib):
     f = binding.forge_paged_gqa_decode_workspace_bytes
-    assert f(32, 32, 8, 128, 512, 512) == ((32 * 32 * 16 * 128 * 4 + 255) // 256) * 256 + 32 * 32 * 16 * 2 * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert f(32, 32, 8, 128, 512, 512) == 65536 * 4 + r256(32 * 32 * 16 * 128 * 4) + 32 * 32 * 16 * 2 * 4
     assert f(4, 8, 2, 64, 4, 1024) == 0      # one split: no scratch
     assert f(4, 8, 2, 64, 4, 17) == 0        # invalid split length
     assert f(-1, 8, 2, 64, 4, 0) == 0

@@ -256,3 +256,26 @@ def test_continuous_batching_36_layer_step():
         assert np.array_equal(bits_host(pool_v[l]), vc_ref)
         err = max_abs_err(outs[l], oracle_decode(wl, t, kc_ref, vc_ref))
         assert err <= TOL["bf16"], f"layer {l}: {err}"
+
+
+def test_one_workspace_serves_changing_shapes():
+    """A workspace zeroed once serves calls of different shapes in any order:
+    split arrival counters live in a fixed prefix that no call's data overlaps."""
+    names = ["skewed", "qwen3_4b", "tiny", "skewed", "qwen3_0_6b", "qwen3_4b"]
+    need = 0
+    for name in set(names):
+        wl = _config(name)[0]
+        need = max(need, binding.forge_paged_gqa_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, wl.MB, 64))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    refs = {}
+    for name in names:
+        wl, t, (kc_ref, vc_ref) = _config(name)
+        if name not in refs:
+            refs[name] = oracle_decode(wl, t, kc_ref, vc_ref)
+        d = DeviceLayer(wl, t)
+        d.append()
+        out = out_tensor(wl)
+        binding.forge_paged_gqa_decode_ex(d.q, d.k_cache, d.v_cache, d.tables, d.lens, wl.scale, out, ws, 64)
+        err = max_abs_err(out, refs[name])
+        assert err <= TOL[wl.spec.out_dtype], f"{name}: {err}"
+    assert_device_clean()

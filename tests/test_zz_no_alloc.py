@@ -64,6 +64,27 @@ def test_noalloc_matches_regular_decode_twice(name):
     assert max_abs_err(first, oracle_decode(wl, t, kc_ref, vc_ref)) <= tol
 
 
+def test_noalloc_alternating_shapes_share_the_scratch():
+    """Calls of different shapes in turn reuse the one static scratch."""
+    lib = binding.load_library()
+    cases = {}
+    for name in ("skewed", "qwen3_0_6b", "qwen3_4b"):
+        wl = W.make_workload(name)
+        t = wl.layer(0)
+        d = DeviceLayer(wl, t)
+        d.append()
+        ref = out_tensor(wl)
+        d.decode(ref)
+        cases[name] = (wl, d, ref)
+    for name in ("qwen3_4b", "skewed", "qwen3_0_6b", "qwen3_4b", "skewed"):
+        wl, d, ref = cases[name]
+        out = out_tensor(wl)
+        assert _call_noalloc(lib, d, out) == 0
+        torch.cuda.synchronize()
+        diff = (out.float() - ref.float()).abs().max().item()
+        assert diff <= TOL[wl.spec.out_dtype], f"{name}: {diff}"
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = binding.load_library()
     spec = W.custom_spec("too_big", B=64, Hq=64, Hkv=8, D=128, fixed_lens=(16384,) * 64, seed=3)
