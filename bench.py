@@ -1,9 +1,12 @@
 #!/usr/bin/env python3
 """Benchmark: one decode step of the paged-KV hot path on GB300.
 
-A step is the whole hot path over one batch: forge_paged_kv_append (scatter
-this step's new K/V token of every sequence into its cache slot) followed by
-forge_paged_gqa_decode (split kernel + split reduce).  The default workload
+A step is the whole hot path over one batch: the scatter of this step's new
+K/V token of every sequence into its cache slot and the paged GQA decode.
+By default a step is one forge_paged_append_gqa_decode launch per layer
+(append fused into the decode kernel); --path separate times
+forge_paged_kv_append followed by forge_paged_gqa_decode, and every run
+reports the other path too.  The default workload
 is the Qwen3-4B-shaped attention layer: batch 32, context lengths uniform in
 [512, 8192], 32 query / 8 KV heads, head_dim 128, 16-token blocks, 10 % free
 blocks interleaved in the pool, bf16 storage.
@@ -147,6 +150,23 @@ def _gpu_id(torch, dev):
         return vis.split(",")[dev] if vis else str(dev)
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of per-rank timings; every rank gets the result.
+    The bench's job time is the slowest rank's (no exchange on the data path)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_gbs(world, bytes_per_step, steps, max_ms):
+    """Whole-job throughput: every rank processes its own batch each step."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 def _seq_bytes(wl, b, out_bytes):
     return wl.Hq * wl.D * 2 + int(wl.context_lens[b]) * wl.Hkv * wl.D * 4 + wl.Hq * wl.D * out_bytes
 
@@ -198,7 +218,8 @@ def cpu_baseline(wl, out_bytes, budget_s=12.0):
         elapsed = time.perf_counter() - t0
     gbs = per_pass * passes / elapsed / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{passes} full pass(es) of the workload (append + decode of all {wl.B} sequences), "
+            "sample": f"{passes} full pass(es) of the workload (append + decode of all {wl.B} sequences"
+                      f"{', layer 0 of ' + str(wl.layers) if wl.layers > 1 else ''}), "
                       f"{elapsed:.1f} s, fp64 C oracle with {threads} threads",
             "ms_per_step": round(1e3 * elapsed / passes, 3)}
 
@@ -265,31 +286,67 @@ def run_native(args, wl, out_bytes):
     torch.cuda.set_device(dev)
     binding.load_library()
 
-    t = wl.layer(0)
-
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
-    host = {"q": bf(t["q"]).pin_memory(), "k_new": bf(t["k_new"]).pin_memory(),
-            "v_new": bf(t["v_new"]).pin_memory(), "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+    # Layers share one block table and one pool [L, NB, Hkv, 16, D]; each
+    # layer has its own q, new K/V row and output.  Single-layer workloads
+    # are the L = 1 case.
+    L = wl.layers
+    host = {"q": torch.empty(L, wl.B, wl.Hq, wl.D, dtype=torch.bfloat16).pin_memory(),
+            "k_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
+            "v_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
+            "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
             "tables": torch.from_numpy(wl.block_tables).pin_memory(),
             "lens": torch.from_numpy(wl.context_lens).pin_memory()}
+    pool_k = torch.empty(L, wl.NB, wl.Hkv, 16, wl.D, dtype=torch.bfloat16, device=dev)
+    pool_v = torch.empty_like(pool_k)
+    for layer in range(L):
+        t = wl.layer(layer)
+        for k in ("q", "k_new", "v_new"):
+            host[k][layer].copy_(bf(t[k]))
+        pool_k[layer].copy_(bf(t["k_cache"]))
+        pool_v[layer].copy_(bf(t["v_cache"]))
+        del t
     d = {k: v.to(dev) for k, v in host.items()}
-    k_cache = bf(t["k_cache"]).to(dev)
-    v_cache = bf(t["v_cache"]).to(dev)
-    del t
     out_dt = torch.bfloat16 if wl.spec.out_dtype == "bf16" else torch.float32
-    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=out_dt, device=dev)
+    out = torch.empty(L, wl.B, wl.Hq, wl.D, dtype=out_dt, device=dev)
     host_out = torch.empty(out.shape, dtype=out_dt).pin_memory()
 
     stream = torch.cuda.Stream(device=dev)
-    bytes_step = wl.bytes_decode(out_bytes)
-    launches_per_step = 2  # append + decode (the split merge runs inside the decode kernel)
+    bytes_layer = wl.bytes_decode(out_bytes)
+    bytes_step = L * bytes_layer
+    launches_per_step = 2 * L  # append + decode per layer (the split merge runs inside the decode kernel)
 
-    def step():
-        binding.forge_paged_kv_append(d["k_new"], d["v_new"], d["slots"], k_cache, v_cache, stream=stream)
-        binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale, out,
-                                       stream=stream)
+    def decode(layer):
+        binding.forge_paged_gqa_decode(d["q"][layer], pool_k[layer], pool_v[layer], d["tables"], d["lens"], wl.scale,
+                                       out[layer], stream=stream)
+
+    def append(layer):
+        binding.forge_paged_kv_append(d["k_new"][layer], d["v_new"][layer], d["slots"], pool_k[layer], pool_v[layer],
+                                      stream=stream)
+
+    def fused(layer):
+        binding.forge_paged_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer], pool_k[layer],
+                                              pool_v[layer], d["tables"], d["lens"], wl.scale, out[layer],
+                                              stream=stream)
+
+    def step_separate():  # the two entry points: append, then decode, per layer
+        for layer in range(L):
+            append(layer)
+            decode(layer)
+
+    def step_fused():  # one launch per layer
+        for layer in range(L):
+            fused(layer)
+
+    def decode_only():
+        for layer in range(L):
+            decode(layer)
+
+    step, other = (step_fused, step_separate) if args.path == "fused" else (step_separate, step_fused)
+    kernel_only = step_fused if args.path == "fused" else decode_only
+    launches_per_step = L if args.path == "fused" else 2 * L
 
     def e2e_step():
         for k in ("q", "k_new", "v_new", "slots", "tables", "lens"):
@@ -298,75 +355,67 @@ def run_native(args, wl, out_bytes):
         host_out.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()  # eager calls first: the decode sizes its workspace on this stream
+        for _ in range(3):  # eager calls first: the decode sizes its workspace on this stream
+            step_separate()
+            step_fused()
     stream.synchronize()
     assert binding.forge_paged_get_device_error(stream) == 0
 
-    # The timed loop replays CUDA graphs that each hold `chunk` whole steps
-    # (append + decode), the way a serving loop replays a captured decode
-    # step: no Python or per-call launch overhead between kernels.  With
-    # --no-graphs the loop makes eager C-ABI calls instead.
-    chunk = max(c for c in range(1, 21) if args.steps % c == 0) if args.graphs else 1
-    g_steps = g_dec = None
-    if args.graphs:
-        g_steps, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # The timed loops replay CUDA graphs that each hold `chunk` whole steps,
+    # the way a serving loop replays a captured decode step: no Python or
+    # per-call launch overhead between kernels.  With --no-graphs the loops
+    # make eager C-ABI calls instead.
+    chunk = max(c for c in range(1, max(1, 20 // L) + 1) if args.steps % c == 0) if args.graphs else 1
+
+    def runner(fn):
+        if not args.graphs:
+            return fn
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            with torch.cuda.graph(g_steps, stream=stream):
+            with torch.cuda.graph(g, stream=stream):
                 for _ in range(chunk):
-                    step()
-            with torch.cuda.graph(g_dec, stream=stream):
-                for _ in range(chunk):
-                    binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale,
-                                                   out, stream=stream)
+                    fn()
+        return g.replay
+
+    run_step, run_other, run_kernel = runner(step), runner(other), runner(kernel_only)
     reps = args.steps // chunk
 
-    def run_chunk():
-        if g_steps is not None:
-            g_steps.replay()
-        else:
-            step()
+    def timed(run, n, per_call_events=False):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range((n if per_call_events else 1) + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for r in range(n):
+                run()
+                if per_call_events:
+                    ev[r + 1].record(stream)
+            if not per_call_events:
+                ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup) // chunk + 1):
-            run_chunk()
-    stream.synchronize()
+    for run in (run_step, run_other, run_kernel):
+        timed(run, max(3, args.warmup) // chunk + 1)
 
     # ---------------- timed region (device-resident inputs)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(_gpu_id(torch, dev.index or 0)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     w0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps):
-            run_chunk()
-        end.record(stream)
-    torch.cuda.synchronize(dev)
+    ms_total = timed(run_step, reps)[0]
     w1 = time.time()
     if ws > 1:
         dist.barrier()
-    ms_total = start.elapsed_time(end)
     rows = sampler.stop() if sampler else []
     clocks = ClockSampler.summarize(rows, w0, w1) if sampler else None
 
-    # ---------------- the decode kernel alone, same launch path, events on its stream
+    # ---------------- the other way of running the step, for comparison
+    ms_other = timed(run_other, reps)[0]
+
+    # ---------------- the dominant kernel alone, same launch path, events on its stream
     dec_reps = max(1, min(reps, 2000 // chunk))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(dec_reps + 1)]
-    with torch.cuda.stream(stream):
-        ev[0].record(stream)
-        for r in range(dec_reps):
-            if g_dec is not None:
-                g_dec.replay()
-            else:
-                binding.forge_paged_gqa_decode(d["q"], k_cache, v_cache, d["tables"], d["lens"], wl.scale, out,
-                                               stream=stream)
-            ev[r + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    decode_ms = [ev[r].elapsed_time(ev[r + 1]) / chunk for r in range(dec_reps)]
+    decode_ms = [x / (chunk * L) for x in timed(run_kernel, dec_reps, per_call_events=True)]
 
     # ---------------- end to end: host buffers, copies inside the timed region
     e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,10 +435,7 @@ def run_native(args, wl, out_bytes):
     assert binding.forge_paged_get_device_error(stream) == 0
     assert torch.isfinite(host_out.float()).all()
 
-    if ws > 1:
-        tt = torch.tensor([ms_total, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, e2e_ms = float(tt[0]), float(tt[1])
+    ms_total, e2e_ms, ms_other = max_over_ranks([ms_total, e2e_ms, ms_other], dev)
 
     if rank != 0:
         if ws > 1:
@@ -398,33 +444,41 @@ def run_native(args, wl, out_bytes):
 
     peak, peak_src = _peaks()
     ms_step = ms_total / args.steps
-    value = ws * bytes_step * args.steps / (ms_total * 1e-3) / 1e9
+    value = aggregate_gbs(ws, bytes_step, args.steps, ms_total)
     dec_avg_ms = statistics.fmean(decode_ms)
-    achieved = bytes_step / (dec_avg_ms * 1e-3) / 1e9
+    achieved = bytes_layer / (dec_avg_ms * 1e-3) / 1e9
     traffic = _traffic_from_profile(_decode_source_hash())
     h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k_new", "v_new", "slots", "tables", "lens"))
     d2h = host_out.numel() * host_out.element_size()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_layer_step": round(ms_step * 1e3, 2),
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_layer_step": round(ms_step * 1e3 / L, 2),
         "pct_of_hbm_peak": round(100.0 * value / ws / peak, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
         "config": _config_dict(wl, {"launch": (f"CUDA graphs of {chunk} steps (append + decode) replayed"
                                                if args.graphs else "eager C-ABI calls"),
                                     "l2": "no flush: inputs larger than L2 (KV pool "
-                                          f"{2 * k_cache.numel() * 2 / 1e6:.0f} MB vs 126 MB L2)",
-                                    "bytes_per_step": bytes_step,
+                                          f"{2 * pool_k.numel() * 2 / 1e6:.0f} MB vs 126 MB L2)",
+                                    "layers": L, "bytes_per_step": bytes_step,
                                     "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_gqa_decode_split_kernel (one decode call; split merge inside)",
+                     "kernel": ("paged_gqa_decode_split_kernel with fused append (one launch per layer)"
+                                if args.path == "fused" else
+                                "paged_gqa_decode_split_kernel (one decode call; split merge inside)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),
                      "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src},
-        "e2e": {"value": round(ws * bytes_step * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(ws, bytes_step, args.steps, e2e_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / args.steps, 5)},
         "gpu_launches": launches_per_step * args.steps,
+        "path": ("forge_paged_append_gqa_decode: append + decode in one launch per layer" if args.path == "fused"
+                 else "forge_paged_kv_append then forge_paged_gqa_decode, per layer"),
+        "other_path": {"path": "separate append + decode calls" if args.path == "fused" else "fused call",
+                       "ms_per_step": round(ms_other / args.steps, 5),
+                       "us_per_layer_step": round(ms_other / args.steps * 1e3 / L, 2),
+                       "value": round(aggregate_gbs(ws, bytes_step, args.steps, ms_other), 2)},
         "clocks": clocks,
     }
     if ws > 1:
@@ -440,6 +494,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="qwen3_4b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="fused: forge_paged_append_gqa_decode; separate: append then decode")
     ap.add_argument("--no-graphs", dest="graphs", action="store_false",
                     help="time eager C-ABI calls instead of replaying captured steps")
     args = ap.parse_args(argv)
@@ -448,8 +504,6 @@ def main(argv=None):
 
     from paged_kv_gqa_06_gb300 import workloads as W
     wl = W.make_workload(args.workload)
-    if wl.layers != 1:
-        raise SystemExit("bench.py times single-layer workloads; the 36-layer step is a parity test")
     out_bytes = 4 if wl.spec.out_dtype == "f32" else 2
 
     if args.impl == "reference":

@@ -176,6 +176,30 @@ FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tenso
                               void *stream);
 
 /*
+ * forge_paged_append_gqa_decode -- this step's append and decode in one
+ * launch.  Same result as forge_paged_kv_append with each sequence's new
+ * token at position context_lens[b] - 1 (slot taken from its block table:
+ * block_tables[b][(L_b-1)/BS] * BS + (L_b-1) % BS) followed by
+ * forge_paged_gqa_decode ("Make the Engine Talk", 1.2: each decode pass
+ * adds the one new token to the cache and attends over everything cached).
+ *
+ *   q, k_cache, v_cache, block_tables, context_lens, scale, out, stream:
+ *                  as forge_paged_gqa_decode (caches are written).
+ *   k_new, v_new   bf16 [B, Hkv, D], layout rules of forge_paged_kv_append.
+ *
+ * A sequence with L_b = 0 appends nothing.  The kernel that reads the
+ * sequence's last block writes the new row into it (in shared memory and in
+ * the cache), so no other launch is needed; the block holding position
+ * L_b - 1 must not be read by another sequence of the same call.  Scratch as
+ * in forge_paged_gqa_decode (library-owned).
+ */
+FORGE_API int forge_paged_append_gqa_decode(const forge_tensor *q, const forge_tensor *k_new,
+                                  const forge_tensor *v_new, forge_tensor *k_cache,
+                                  forge_tensor *v_cache, const forge_tensor *block_tables,
+                                  const forge_tensor *context_lens, float scale, forge_tensor *out,
+                                  void *stream);
+
+/*
  * forge_paged_gqa_decode_noalloc -- forge_paged_gqa_decode for callers that
  * must not allocate device memory.  (The pages have no counterpart: this is
  * an entry point of this library only.)

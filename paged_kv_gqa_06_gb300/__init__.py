@@ -19,6 +19,7 @@ from __future__ import annotations
 __all__ = [
     "forge_paged_kv_append",
     "forge_paged_gqa_decode",
+    "forge_paged_append_gqa_decode",
     "forge_paged_gqa_decode_ex",
     "forge_paged_gqa_decode_noalloc",
     "forge_paged_gqa_decode_workspace_bytes",

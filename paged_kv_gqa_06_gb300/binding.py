@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_paged_gqa_decode_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, P, ctypes.c_size_t,
                                                   ctypes.c_int, P]
         lib.forge_paged_gqa_decode_ex.restype = ctypes.c_int
+        lib.forge_paged_append_gqa_decode.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, T, P]
+        lib.forge_paged_append_gqa_decode.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_noalloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, P]
         lib.forge_paged_gqa_decode_noalloc.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
@@ -144,6 +146,18 @@ def forge_paged_gqa_decode(q, k_cache, v_cache, block_tables, context_lens, scal
                                     _ref(describe(block_tables)), _ref(describe(context_lens)),
                                     float(scale), _ref(describe(out)), _stream_ptr(stream))
     _raise(rc, "forge_paged_gqa_decode")
+    return out
+
+
+def forge_paged_append_gqa_decode(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                  stream=None):
+    """Append each sequence's new K/V at position L-1 and decode, in one launch."""
+    lib = load_library()
+    rc = lib.forge_paged_append_gqa_decode(_ref(describe(q)), _ref(describe(k_new)), _ref(describe(v_new)),
+                                           _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                           _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                           float(scale), _ref(describe(out)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_append_gqa_decode")
     return out
 
 

@@ -421,6 +421,40 @@ int forge_paged_gqa_decode(const forge_tensor* q, const forge_tensor* k_cache, c
   return launch_plan(&plan, static_cast<cudaStream_t>(stream));
 }
 
+int forge_paged_append_gqa_decode(const forge_tensor* q, const forge_tensor* k_new, const forge_tensor* v_new,
+                                  forge_tensor* k_cache, forge_tensor* v_cache, const forge_tensor* block_tables,
+                                  const forge_tensor* context_lens, float scale, forge_tensor* out, void* stream) {
+  DecodePlan plan;
+  FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, 148, &plan));
+  FORGE_TRY(check_tensor(k_new, FORGE_BF16, 3));
+  FORGE_TRY(check_tensor(v_new, FORGE_BF16, 3));
+  for (int i = 0; i < 3; ++i)
+    if (v_new->shape[i] != k_new->shape[i]) return FORGE_ERR_SHAPE;
+  if (k_new->shape[0] != q->shape[0] || k_new->shape[1] != k_cache->shape[1] || k_new->shape[2] != q->shape[2])
+    return FORGE_ERR_SHAPE;
+  if (plan.p.B == 0) return FORGE_OK;
+  FORGE_TRY(check_vec16(k_new, 2));
+  FORGE_TRY(check_vec16(v_new, 2));
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+  FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, sms, &plan));
+  void* ws = nullptr;
+  if (plan.ws_bytes > 0) FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws));
+  plan.p.err = err;
+  plan.p.k_new = static_cast<const __nv_bfloat16*>(k_new->data);
+  plan.p.v_new = static_cast<const __nv_bfloat16*>(v_new->data);
+  plan.p.kn_sb = k_new->stride[0];
+  plan.p.kn_sh = k_new->stride[1];
+  plan.p.vn_sb = v_new->stride[0];
+  plan.p.vn_sh = v_new->stride[1];
+  plan.p.k_cache_w = static_cast<__nv_bfloat16*>(k_cache->data);
+  plan.p.v_cache_w = static_cast<__nv_bfloat16*>(v_cache->data);
+  attach_workspace(&plan, ws);
+  return launch_plan(&plan, static_cast<cudaStream_t>(stream));
+}
+
 const char* forge_status_string(int status) {
   switch (status) {
     case FORGE_OK: return "FORGE_OK";

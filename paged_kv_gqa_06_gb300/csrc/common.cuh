@@ -57,6 +57,13 @@ struct DecodeParams {
   int s_max;       // split slots per (b, h) in the workspace
   int nstage;      // shared-memory ring depth (pipeline stages)
   float qk_scale_log2;  // scale * log2(e): logits come out in log2 units
+  // Fused append (all null for a plain decode): the new K/V row of sequence
+  // b, KV head g, written at position L_b - 1 of the cache before use.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t kn_sb, kn_sh, vn_sb, vn_sh;
+  __nv_bfloat16* k_cache_w;
+  __nv_bfloat16* v_cache_w;
   int* err;
 };
 

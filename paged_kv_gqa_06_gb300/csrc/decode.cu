@@ -99,6 +99,22 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
   return tile + (chunk >> 3) * kBoxBytes + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
 }
 
+// Fused append: put this step's new row (`src`, D bf16) into row `r` of the
+// staged swizzled tile at `tile`, and into the cache row `cache_row` (when
+// not null), 16 bytes per lane.  Then order the shared-memory writes before
+// the warp's ldmatrix reads and before the TMA engine reuses the stage.
+template <int D>
+__device__ __forceinline__ void patch_new_row(unsigned char* tile, const __nv_bfloat16* src,
+                                              __nv_bfloat16* cache_row, int r, int lane) {
+  for (int c = lane; c < D / 8; c += 32) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    if (cache_row) reinterpret_cast<uint4*>(cache_row)[c] = v;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
 // x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -336,6 +352,20 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     }
   }
 
+  // Fused append: the split holding position L-1 patches that row of its last
+  // block with this step's new K (pass 1) and V (pass 2), and stores it.
+  const bool fused = p.k_new != nullptr && s == nsplit - 1;
+  const int jl = n - 1, rl = (L - 1) % kBlockSize;  // block within the split, row
+  __nv_bfloat16* kdst = nullptr;
+  __nv_bfloat16* vdst = nullptr;
+  if (fused) {
+    const int pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0 + jl);
+    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.NB)) {  // a bad id is recorded by the producer
+      kdst = p.k_cache_w + static_cast<int64_t>(pb) * p.kc_sblk + g * p.kc_sh + rl * D;
+      vdst = p.v_cache_w + static_cast<int64_t>(pb) * p.vc_sblk + g * p.vc_sh + rl * D;
+    }
+  }
+
   int slot = 0;
   uint32_t phase = 0;
 
@@ -345,6 +375,9 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     const int j = st * kStageBlocks + warp;  // block within the split
     if (j < n) {
       const uint32_t tile = ring_s + (slot * kStageBlocks + warp) * TILE_BYTES;
+      if (fused && j == jl)
+        patch_new_row<D>(ring + (slot * kStageBlocks + warp) * TILE_BYTES,
+                         p.k_new + static_cast<int64_t>(b) * p.kn_sb + g * p.kn_sh, kdst, rl, lane);
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // token row this lane addresses
       const int acol = lane >> 4;                           // +0 / +1 chunk
@@ -438,6 +471,9 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
         fence_proxy_async_smem();  // before the TMA engine refills this stage
         __syncwarp();
       }
+      if (fused && j == jl)
+        patch_new_row<D>(ring + (slot * kStageBlocks + warp) * TILE_BYTES,
+                         p.v_new + static_cast<int64_t>(b) * p.vn_sb + g * p.vn_sh, vdst, rl, lane);
       // B operand P^T (k = token, n = head): {p[tq][2tr], +1}, {p[tq][8 + 2tr], +1}
       uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
       if (tq < G) {

@@ -149,3 +149,18 @@ def test_python_binding_raises_on_bad_status(lib):
         binding.forge_paged_gqa_decode(q, kc, kc, torch.zeros(2, 4, dtype=torch.int32),
                                        torch.zeros(2, dtype=torch.int32), 0.1, out, stream=0)
     assert e.value.status == -4
+
+
+def test_fused_entry_rejects_bad_new_rows(lib):
+    a = _decode_args()
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    good = _desc([2, 2, 64], BF16)
+
+    def call(kn, vn):
+        return lib.forge_paged_append_gqa_decode(r(a["q"]), r(kn), r(vn), r(a["k"]), r(a["v"]), r(a["bt"]),
+                                                 r(a["cl"]), a["scale"], r(a["out"]), None)
+    assert call(None, good) == -1
+    assert call(_desc([2, 2, 64], F32), good) == -2
+    assert call(good, _desc([2, 3, 64], BF16)) == -3
+    assert call(_desc([3, 2, 64], BF16), _desc([3, 2, 64], BF16)) == -3
+    assert call(_desc([2, 2, 64], BF16, data=8), good) == -5

@@ -1,0 +1,65 @@
+"""The bench's multi-rank path on CPU: two gloo ranks, one process each.
+
+The path has no exchange step (replicas only); what crosses ranks is the
+timing: the job time is the slowest rank's, and the whole-job throughput
+counts every rank's batch.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank r took (r + 1) ms for the device loop and (10 - r) ms end to end
+    got = bench.max_over_ranks([rank + 1.0, 10.0 - rank])
+    results[rank] = got
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        mp.start_processes(_rank_main, args=(world, _free_port(), results), nprocs=world, join=True,
+                           start_method="spawn")
+        assert dict(results) == {0: [2.0, 10.0], 1: [2.0, 10.0]}
+
+
+def test_whole_job_throughput_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    one = bench.aggregate_gbs(1, 1e9, 10, 1000.0)     # 10 GB in 1 s
+    assert one == pytest.approx(10.0)
+    assert bench.aggregate_gbs(4, 1e9, 10, 1000.0) == pytest.approx(40.0)
+    assert bench.max_over_ranks([3.0, 1.0]) == [3.0, 1.0]   # no process group: unchanged
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_gqa_06_gb300 import workloads as W
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        steps, warmup = 3, 3
+    assert bench.run_reference(Args(), W.make_workload("tiny"), 4) is None
