@@ -17,8 +17,9 @@ Citations (page title, section):
     attention.
 
 Pins: every function here is pinned by CPU tests against brute-force dense
-attention, torch's scaled_dot_product_attention in fp64, closed forms and
-invariants (see ``tests/test_oracle_pins.py``).
+attention, torch's scaled_dot_product_attention in fp64, closed forms,
+hand-derived examples and invariants (``tests/test_oracle_pins.py``,
+``tests/test_oracle_qk_pins.py``).
 """
 from __future__ import annotations
 
@@ -76,6 +77,10 @@ def _load():
             lib.oracle_paged_gqa_decode.argtypes = [P, P, P, P, P, ctypes.c_double, P,
                                                     i, i, i, i, i, i, i, i]
             lib.oracle_paged_gqa_decode.restype = i
+            lib.oracle_rmsnorm.argtypes = [P, P, ctypes.c_double, P, i, i]
+            lib.oracle_rmsnorm.restype = None
+            lib.oracle_rope.argtypes = [P, P, ctypes.c_double, i, i]
+            lib.oracle_rope.restype = None
             _lib = lib
     return _lib
 
@@ -144,3 +149,45 @@ def paged_gqa_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
                                          B, Hq, Hkv, D, NB, BS, MB, int(nthreads))
     _check(rc, "decode")
     return out
+
+
+def rmsnorm(x, weight, eps) -> np.ndarray:
+    """fp64 RMSNorm of each last-axis row of x (bf16 bits); weight [D] bf16 bits or None."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    D = x.shape[-1]
+    rows = x.size // D
+    y = np.empty(x.shape, dtype=np.float64)
+    w = None if weight is None else np.ascontiguousarray(weight, dtype=np.uint16)
+    _load().oracle_rmsnorm(_ptr(x), None if w is None else _ptr(w), float(eps), _ptr(y), rows, D)
+    return y
+
+
+def rope(x, positions, theta) -> np.ndarray:
+    """Rotate-half rotary embedding of fp64 rows x [..., D] at per-row positions
+    (broadcast over the rows of each leading index); returns a new array."""
+    x = np.array(x, dtype=np.float64, order="C", copy=True)
+    D = x.shape[-1]
+    rows = x.size // D
+    pos = np.ascontiguousarray(np.broadcast_to(np.asarray(positions, dtype=np.int64).reshape(
+        np.asarray(positions).shape + (1,) * (x.ndim - 1 - np.asarray(positions).ndim)), x.shape[:-1]),
+        dtype=np.int64).reshape(rows)
+    _load().oracle_rope(_ptr(x), _ptr(pos), float(theta), rows, D)
+    return x
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round fp64 values straight to bf16 (nearest, ties to even) and return the
+    bf16 bits.  Rounding via float32 first could round twice; this takes the
+    8-bit quantum of each value's binade directly.  Normal-range values only."""
+    x = np.asarray(x, dtype=np.float64)
+    b = x.view(np.uint64)
+    sign = (b >> np.uint64(63)).astype(np.uint16)
+    a = np.abs(x)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    nz = a > 0
+    m, e = np.frexp(a[nz])                    # a = m * 2^e, m in [0.5, 1)
+    # bf16 normal: 8 significant bits -> quantum 2^(e-8) for |x| in [2^(e-1), 2^e)
+    q = np.ldexp(np.ones_like(m), e - 8)
+    r = np.rint(a[nz] / q) * q                # rint: ties to even
+    out[nz] = (np.asarray(r, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return out | (sign << np.uint16(15))

@@ -74,6 +74,48 @@ int oracle_paged_kv_append(const uint16_t *k_new, const uint16_t *v_new,
     return ORACLE_OK;
 }
 
+/*
+ * RMSNorm of each row of x ([rows, D], bf16 bits) with weight w ([D], bf16
+ * bits; NULL = all ones), in fp64:  y = x / sqrt(mean(x^2) + eps) * w.
+ * ("Make the Engine Talk", 1.3: RMSNorm is one of the forward pass's
+ * mechanisms; here it is applied per attention head to q and k.)
+ */
+void oracle_rmsnorm(const uint16_t *x, const uint16_t *w, double eps, double *y, int rows, int D) {
+    for (int r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int d = 0; d < D; ++d) {
+            double v = bf16_bits_to_double(x[(size_t)r * D + d]);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / D + eps);
+        for (int d = 0; d < D; ++d) {
+            double wd = w ? bf16_bits_to_double(w[d]) : 1.0;
+            y[(size_t)r * D + d] = bf16_bits_to_double(x[(size_t)r * D + d]) * inv * wd;
+        }
+    }
+}
+
+/*
+ * Rotary position embedding, rotate-half form, in place on fp64 rows
+ * ([rows, D]) at positions pos[r] ("Make the Engine Talk", 1.3: rotary
+ * position embeddings).  For i < D/2, with angle a = pos * theta^(-2i/D):
+ *   y[i]       = x[i] cos a - x[i+D/2] sin a
+ *   y[i+D/2]   = x[i+D/2] cos a + x[i] sin a
+ */
+void oracle_rope(double *x, const int64_t *pos, double theta, int rows, int D) {
+    const int h = D / 2;
+    for (int r = 0; r < rows; ++r) {
+        double *row = x + (size_t)r * D;
+        for (int i = 0; i < h; ++i) {
+            double a = (double)pos[r] * pow(theta, -2.0 * i / D);
+            double c = cos(a), s = sin(a);
+            double x1 = row[i], x2 = row[i + h];
+            row[i] = x1 * c - x2 * s;
+            row[i + h] = x2 * c + x1 * s;
+        }
+    }
+}
+
 typedef struct {
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
