@@ -86,6 +86,7 @@ typedef enum {
 #define FORGE_DEVERR_LENGTH 2     /* context_lens[b] > MB * BS (or negative) */
 #define FORGE_DEVERR_SLOT 3       /* slot_mapping[b] >= NB * BS */
 #define FORGE_DEVERR_TIMEOUT 4    /* a pipeline wait gave up (should never happen) */
+#define FORGE_DEVERR_POSITION 5   /* context_lens[b] - 1 beyond the rotary table (rotation skipped) */
 
 /*
  * forge_paged_kv_append -- write this step's new K/V token of every sequence
@@ -198,6 +199,53 @@ FORGE_API int forge_paged_append_gqa_decode(const forge_tensor *q, const forge_t
                                   forge_tensor *v_cache, const forge_tensor *block_tables,
                                   const forge_tensor *context_lens, float scale, forge_tensor *out,
                                   void *stream);
+
+/*
+ * The q/k path before attention ("Make the Engine Talk", 1.3: RMSNorm and
+ * rotary position embeddings are mechanisms of the forward pass), applied to
+ * each query head row and to each new key row of the fused call below, at the
+ * new token's position pos = context_lens[b] - 1:
+ *   x <- x / sqrt(mean(x^2) + norm_eps) * weight          (when a weight is set)
+ *   for i < D/2, with (c, s) = rope_cos_sin[pos][i], [pos][D/2 + i]:
+ *     x[i] <- x[i] c - x[i + D/2] s,  x[i + D/2] <- x[i + D/2] c + x[i] s
+ * computed in fp32 and rounded once to bf16.  The rotated key is what the
+ * cache stores.
+ *
+ *   q_norm_weight,
+ *   k_norm_weight  bf16 [D], contiguous, or NULL (no RMSNorm on that side).
+ *   norm_eps       >= 0, finite (used when a weight is set).
+ *   rope_cos_sin   f32 [P, D], contiguous: cos of pos * theta^(-2i/D) in
+ *                  columns [0, D/2), sin in [D/2, D); see
+ *                  forge_rope_cos_sin_table.  NULL: no rotation.  A position
+ *                  >= P skips the rotation and records FORGE_DEVERR_POSITION.
+ */
+typedef struct {
+    const forge_tensor *q_norm_weight;
+    const forge_tensor *k_norm_weight;
+    float norm_eps;
+    const forge_tensor *rope_cos_sin;
+} forge_qk_options;
+
+/*
+ * forge_paged_qk_append_gqa_decode -- forge_paged_append_gqa_decode with the
+ * q/k path above applied to q and k_new inside the same launch (qk may be
+ * NULL: then identical to forge_paged_append_gqa_decode).
+ */
+FORGE_API int forge_paged_qk_append_gqa_decode(const forge_tensor *q, const forge_tensor *k_new,
+                                     const forge_tensor *v_new, const forge_qk_options *qk,
+                                     forge_tensor *k_cache, forge_tensor *v_cache,
+                                     const forge_tensor *block_tables,
+                                     const forge_tensor *context_lens, float scale,
+                                     forge_tensor *out, void *stream);
+
+/*
+ * Fill out[rows * D] (host memory, f32) with the rotary table for
+ * forge_qk_options.rope_cos_sin: out[r][i] = cos(r * theta^(-2i/D)) and
+ * out[r][D/2 + i] = sin(r * theta^(-2i/D)) for i < D/2, computed in double.
+ * Host-only, no CUDA call.  FORGE_ERR_VALUE for D odd or <= 0, rows <= 0 or
+ * theta <= 0.
+ */
+FORGE_API int forge_rope_cos_sin_table(double theta, int D, int rows, float *out);
 
 /*
  * forge_paged_gqa_decode_noalloc -- forge_paged_gqa_decode for callers that

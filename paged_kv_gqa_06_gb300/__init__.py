@@ -20,6 +20,8 @@ __all__ = [
     "forge_paged_kv_append",
     "forge_paged_gqa_decode",
     "forge_paged_append_gqa_decode",
+    "forge_paged_qk_append_gqa_decode",
+    "forge_rope_cos_sin_table",
     "forge_paged_gqa_decode_ex",
     "forge_paged_gqa_decode_noalloc",
     "forge_paged_gqa_decode_workspace_bytes",

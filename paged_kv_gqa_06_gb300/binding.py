@@ -27,12 +27,17 @@ STATUS_NAMES = {0: "FORGE_OK", -1: "FORGE_ERR_NULL", -2: "FORGE_ERR_DTYPE", -3: 
                 -4: "FORGE_ERR_UNSUPPORTED", -5: "FORGE_ERR_ALIGN", -6: "FORGE_ERR_CUDA",
                 -7: "FORGE_ERR_WORKSPACE", -8: "FORGE_ERR_VALUE"}
 DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "context length longer than the table row",
-                 3: "slot outside the pool", 4: "pipeline wait timed out"}
+                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "position beyond the rotary table"}
 
 
 class ForgeTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class ForgeQKOptions(ctypes.Structure):
+    _fields_ = [("q_norm_weight", ctypes.POINTER(ForgeTensor)), ("k_norm_weight", ctypes.POINTER(ForgeTensor)),
+                ("norm_eps", ctypes.c_float), ("rope_cos_sin", ctypes.POINTER(ForgeTensor))]
 
 
 class ForgeError(RuntimeError):
@@ -65,6 +70,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_paged_gqa_decode_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, P, ctypes.c_size_t,
                                                   ctypes.c_int, P]
         lib.forge_paged_gqa_decode_ex.restype = ctypes.c_int
+        lib.forge_paged_qk_append_gqa_decode.argtypes = [T, T, T, ctypes.POINTER(ForgeQKOptions), T, T, T, T,
+                                                         ctypes.c_float, T, P]
+        lib.forge_paged_qk_append_gqa_decode.restype = ctypes.c_int
+        lib.forge_rope_cos_sin_table.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_float)]
+        lib.forge_rope_cos_sin_table.restype = ctypes.c_int
         lib.forge_paged_append_gqa_decode.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, T, P]
         lib.forge_paged_append_gqa_decode.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_noalloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, P]
@@ -159,6 +170,39 @@ def forge_paged_append_gqa_decode(q, k_new, v_new, k_cache, v_cache, block_table
                                            float(scale), _ref(describe(out)), _stream_ptr(stream))
     _raise(rc, "forge_paged_append_gqa_decode")
     return out
+
+
+def qk_options(q_norm_weight=None, k_norm_weight=None, norm_eps=1e-6, rope_cos_sin=None) -> ForgeQKOptions:
+    """forge_qk_options for forge_paged_qk_append_gqa_decode (tensors may be None)."""
+    o = ForgeQKOptions()
+    o.norm_eps = float(norm_eps)
+    for name, t in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight),
+                    ("rope_cos_sin", rope_cos_sin)):
+        setattr(o, name, ctypes.pointer(describe(t)) if t is not None else None)
+    return o
+
+
+def forge_paged_qk_append_gqa_decode(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                     q_norm_weight=None, k_norm_weight=None, norm_eps=1e-6, rope_cos_sin=None,
+                                     stream=None):
+    """Append + decode in one launch, with RMSNorm / RoPE on q and the new k first."""
+    lib = load_library()
+    o = qk_options(q_norm_weight, k_norm_weight, norm_eps, rope_cos_sin)
+    rc = lib.forge_paged_qk_append_gqa_decode(_ref(describe(q)), _ref(describe(k_new)), _ref(describe(v_new)),
+                                              ctypes.byref(o), _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                              _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                              float(scale), _ref(describe(out)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_qk_append_gqa_decode")
+    return out
+
+
+def forge_rope_cos_sin_table(theta: float, D: int, rows: int) -> torch.Tensor:
+    """The rotary cos/sin table [rows, D] (f32, host) built by the library."""
+    t = torch.empty(rows, D, dtype=torch.float32)
+    rc = load_library().forge_rope_cos_sin_table(float(theta), int(D), int(rows),
+                                                 ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_float)))
+    _raise(rc, "forge_rope_cos_sin_table")
+    return t
 
 
 def forge_paged_gqa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):

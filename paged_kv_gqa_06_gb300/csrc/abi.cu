@@ -421,9 +421,74 @@ int forge_paged_gqa_decode(const forge_tensor* q, const forge_tensor* k_cache, c
   return launch_plan(&plan, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// Validates the optional q/k path arguments against head size D.
+int check_qk_options(const forge_qk_options* o, int64_t D) {
+  if (!o) return FORGE_OK;
+  for (const forge_tensor* w : {o->q_norm_weight, o->k_norm_weight}) {
+    if (!w) continue;
+    FORGE_TRY(check_tensor(w, FORGE_BF16, 1));
+    if (w->shape[0] != D) return FORGE_ERR_SHAPE;
+    if (!w->data) return FORGE_ERR_NULL;
+    if (w->stride[0] != 1) return FORGE_ERR_SHAPE;
+  }
+  if ((o->q_norm_weight || o->k_norm_weight) && !(std::isfinite(o->norm_eps) && o->norm_eps >= 0.f))
+    return FORGE_ERR_VALUE;
+  if (o->rope_cos_sin) {
+    const forge_tensor* r = o->rope_cos_sin;
+    FORGE_TRY(check_tensor(r, FORGE_F32, 2));
+    if (r->shape[1] != D || r->shape[0] < 1 || r->shape[0] > INT32_MAX) return FORGE_ERR_SHAPE;
+    if (!r->data) return FORGE_ERR_NULL;
+    if (r->stride[1] != 1 || r->stride[0] != D) return FORGE_ERR_SHAPE;
+  }
+  return FORGE_OK;
+}
+
+int append_decode_impl(const forge_tensor* q, const forge_tensor* k_new, const forge_tensor* v_new,
+                       const forge_qk_options* qk, forge_tensor* k_cache, forge_tensor* v_cache,
+                       const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                       forge_tensor* out, void* stream);
+
+}  // namespace
+
+int forge_paged_qk_append_gqa_decode(const forge_tensor* q, const forge_tensor* k_new, const forge_tensor* v_new,
+                                     const forge_qk_options* qk, forge_tensor* k_cache, forge_tensor* v_cache,
+                                     const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                                     forge_tensor* out, void* stream) {
+  return append_decode_impl(q, k_new, v_new, qk, k_cache, v_cache, block_tables, context_lens, scale, out, stream);
+}
+
+int forge_rope_cos_sin_table(double theta, int D, int rows, float* out) {
+  if (!out) return FORGE_ERR_NULL;
+  if (D <= 0 || D % 2 != 0 || rows <= 0 || !(theta > 0.0)) return FORGE_ERR_VALUE;
+  const int h = D / 2;
+  for (int i = 0; i < h; ++i) {
+    const double inv_freq = std::pow(theta, -2.0 * i / D);
+    for (int r = 0; r < rows; ++r) {
+      const double a = static_cast<double>(r) * inv_freq;
+      out[static_cast<size_t>(r) * D + i] = static_cast<float>(std::cos(a));
+      out[static_cast<size_t>(r) * D + h + i] = static_cast<float>(std::sin(a));
+    }
+  }
+  return FORGE_OK;
+}
+
 int forge_paged_append_gqa_decode(const forge_tensor* q, const forge_tensor* k_new, const forge_tensor* v_new,
                                   forge_tensor* k_cache, forge_tensor* v_cache, const forge_tensor* block_tables,
                                   const forge_tensor* context_lens, float scale, forge_tensor* out, void* stream) {
+  return append_decode_impl(q, k_new, v_new, nullptr, k_cache, v_cache, block_tables, context_lens, scale, out,
+                            stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int append_decode_impl(const forge_tensor* q, const forge_tensor* k_new, const forge_tensor* v_new,
+                       const forge_qk_options* qk, forge_tensor* k_cache, forge_tensor* v_cache,
+                       const forge_tensor* block_tables, const forge_tensor* context_lens, float scale,
+                       forge_tensor* out, void* stream) {
   DecodePlan plan;
   FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, 148, &plan));
   FORGE_TRY(check_tensor(k_new, FORGE_BF16, 3));
@@ -432,6 +497,7 @@ int forge_paged_append_gqa_decode(const forge_tensor* q, const forge_tensor* k_n
     if (v_new->shape[i] != k_new->shape[i]) return FORGE_ERR_SHAPE;
   if (k_new->shape[0] != q->shape[0] || k_new->shape[1] != k_cache->shape[1] || k_new->shape[2] != q->shape[2])
     return FORGE_ERR_SHAPE;
+  FORGE_TRY(check_qk_options(qk, q->shape[2]));
   if (plan.p.B == 0) return FORGE_OK;
   FORGE_TRY(check_vec16(k_new, 2));
   FORGE_TRY(check_vec16(v_new, 2));
@@ -451,9 +517,22 @@ int forge_paged_append_gqa_decode(const forge_tensor* q, const forge_tensor* k_n
   plan.p.vn_sh = v_new->stride[1];
   plan.p.k_cache_w = static_cast<__nv_bfloat16*>(k_cache->data);
   plan.p.v_cache_w = static_cast<__nv_bfloat16*>(v_cache->data);
+  if (qk) {
+    if (qk->q_norm_weight) plan.p.q_norm_w = static_cast<const __nv_bfloat16*>(qk->q_norm_weight->data);
+    if (qk->k_norm_weight) plan.p.k_norm_w = static_cast<const __nv_bfloat16*>(qk->k_norm_weight->data);
+    plan.p.norm_eps = qk->norm_eps;
+    if (qk->rope_cos_sin) {
+      plan.p.rope = static_cast<const float*>(qk->rope_cos_sin->data);
+      plan.p.rope_rows = static_cast<int>(qk->rope_cos_sin->shape[0]);
+    }
+  }
   attach_workspace(&plan, ws);
   return launch_plan(&plan, static_cast<cudaStream_t>(stream));
 }
+
+}  // namespace
+
+extern "C" {
 
 const char* forge_status_string(int status) {
   switch (status) {

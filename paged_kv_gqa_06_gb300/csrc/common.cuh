@@ -20,6 +20,7 @@ constexpr int kDevErrBlockId = 1;
 constexpr int kDevErrLength = 2;
 constexpr int kDevErrSlot = 3;
 constexpr int kDevErrTimeout = 4;
+constexpr int kDevErrPosition = 5;
 
 // A wait on a pipeline barrier gives up after this long (ns of %globaltimer).
 // A copy of a few KiB completes in microseconds; reaching this means a bug,
@@ -64,6 +65,15 @@ struct DecodeParams {
   int64_t kn_sb, kn_sh, vn_sb, vn_sh;
   __nv_bfloat16* k_cache_w;
   __nv_bfloat16* v_cache_w;
+  // Optional q/k path of the fused call (all null = none): per-head RMSNorm
+  // weights [D] and rotary cos/sin rows [rope_rows, D] (cos in [0, D/2),
+  // sin in [D/2, D)), applied at position L_b - 1 before q and the new k
+  // are used (and k is stored).
+  const __nv_bfloat16* q_norm_w;
+  const __nv_bfloat16* k_norm_w;
+  float norm_eps;
+  const float* rope;
+  int rope_rows;
   int* err;
 };
 

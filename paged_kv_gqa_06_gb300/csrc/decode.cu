@@ -115,6 +115,111 @@ __device__ __forceinline__ void patch_new_row(unsigned char* tile, const __nv_bf
   __syncwarp();
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The q/k path ("Make the Engine Talk", 1.3: RMSNorm and rotary position
+// embeddings), for the q fragments of one head held by the 4 lanes of an MMA
+// group: x[ks][e] is dim 16 ks + 2 tr + e (e < 2) or 16 ks + 8 + 2 tr + e - 2
+// (e >= 2).  RMSNorm with weight w_q (sum of squares over the 4 lanes), then
+// rotate-half RoPE at `pos`: dim d < D/2 pairs with d + D/2, which is slot
+// ks + D/32 of the same lane.  fp32 throughout.
+template <int D>
+__device__ __forceinline__ void q_norm_rope(float (&x)[D / 16][4], int tr, const DecodeParams& p, int pos,
+                                            bool rope) {
+  constexpr int K = D / 16;
+  auto dim = [&](int ks, int e) { return 16 * ks + (e < 2 ? 2 * tr + e : 8 + 2 * tr + e - 2); };
+  if (p.q_norm_w) {
+    float ss = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < K; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(x[ks][e], x[ks][e], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float inv = rsqrtf(ss / D + p.norm_eps);
+#pragma unroll
+    for (int ks = 0; ks < K; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[ks][e] *= inv * __bfloat162float(p.q_norm_w[dim(ks, e)]);
+  }
+  if (rope) {
+    const float* cs = p.rope + static_cast<int64_t>(pos) * D;
+#pragma unroll
+    for (int ks = 0; ks < K / 2; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = dim(ks, e);
+        const float c = __ldg(cs + d), sn = __ldg(cs + D / 2 + d);
+        const float x1 = x[ks][e], x2 = x[ks + K / 2][e];
+        x[ks][e] = x1 * c - x2 * sn;
+        x[ks + K / 2][e] = x2 * c + x1 * sn;
+      }
+  }
+}
+
+// Fused append with the q/k path: the new K row (`src`) through RMSNorm
+// (weight w_k) and RoPE at `pos`, rounded once to bf16, into row `r` of the
+// staged tile and into the cache row.  Lane c < D/8 holds dims 8c .. 8c+7;
+// its rotation partner (dims D/2 away) is lane c ^ (D/16).
+template <int D>
+__device__ __forceinline__ void patch_new_k_row(unsigned char* tile, const __nv_bfloat16* src,
+                                                __nv_bfloat16* cache_row, int r, int lane, const DecodeParams& p,
+                                                int pos, bool rope) {
+  constexpr int C = D / 8;
+  const bool has = lane < C;
+  float x[8];
+  if (has) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = bf16lo(w[k]);
+      x[2 * k + 1] = bf16hi(w[k]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  }
+  if (p.k_norm_w) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = rsqrtf(ss / D + p.norm_eps);
+    if (has) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= inv * __bfloat162float(p.k_norm_w[8 * lane + e]);
+    }
+  }
+  if (rope) {
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], C / 2);
+    if (has) {
+      const bool first = lane < C / 2;
+      const int d0 = 8 * (first ? lane : lane - C / 2);  // rotation index of this lane's dims
+      const float* cs = p.rope + static_cast<int64_t>(pos) * D;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float c = __ldg(cs + d0 + e), sn = __ldg(cs + D / 2 + d0 + e);
+        x[e] = first ? x[e] * c - y[e] * sn : x[e] * c + y[e] * sn;
+      }
+    }
+  }
+  if (has) {
+    const uint4 v = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                               pack_bf16x2(x[6], x[7]));
+    *reinterpret_cast<uint4*>(tile + (lane >> 3) * kBoxBytes + r * 128 + (((lane & 7) ^ (r & 7)) << 4)) = v;
+    if (cache_row) reinterpret_cast<uint4*>(cache_row)[lane] = v;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
 // x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -342,6 +447,11 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
 
   // B operand of the QK product, q^T (k = dim, n = head), for all KSTEPS:
   // {q[tq][16ks + 2tr], +1} and {q[tq][16ks + 8 + 2tr], +1}; heads >= G are 0.
+  // The optional q/k path runs at position L-1 (the new token's).
+  const int pos = L - 1;
+  const bool qk_path = p.q_norm_w != nullptr || p.k_norm_w != nullptr || p.rope != nullptr;
+  const bool rope = p.rope != nullptr && pos < p.rope_rows;
+  if (p.rope != nullptr && !rope && tid == 0 && s == 0 && g == 0) record_error(p.err, kDevErrPosition);
   uint32_t qb[KSTEPS][2];
   {
     const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + tq) * p.q_sh;
@@ -349,6 +459,22 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     for (int ks = 0; ks < KSTEPS; ++ks) {
       qb[ks][0] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
       qb[ks][1] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
+    }
+    if (qk_path) {  // uniform across the CTA
+      float x[KSTEPS][4];
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        x[ks][0] = bf16lo(qb[ks][0]);
+        x[ks][1] = bf16hi(qb[ks][0]);
+        x[ks][2] = bf16lo(qb[ks][1]);
+        x[ks][3] = bf16hi(qb[ks][1]);
+      }
+      q_norm_rope<D>(x, tr, p, pos, rope);
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        qb[ks][0] = tq < G ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
+        qb[ks][1] = tq < G ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
+      }
     }
   }
 
@@ -375,9 +501,14 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
     const int j = st * kStageBlocks + warp;  // block within the split
     if (j < n) {
       const uint32_t tile = ring_s + (slot * kStageBlocks + warp) * TILE_BYTES;
-      if (fused && j == jl)
-        patch_new_row<D>(ring + (slot * kStageBlocks + warp) * TILE_BYTES,
-                         p.k_new + static_cast<int64_t>(b) * p.kn_sb + g * p.kn_sh, kdst, rl, lane);
+      if (fused && j == jl) {
+        unsigned char* t = ring + (slot * kStageBlocks + warp) * TILE_BYTES;
+        const __nv_bfloat16* src = p.k_new + static_cast<int64_t>(b) * p.kn_sb + g * p.kn_sh;
+        if (qk_path)
+          patch_new_k_row<D>(t, src, kdst, rl, lane, p, pos, rope);
+        else
+          patch_new_row<D>(t, src, kdst, rl, lane);
+      }
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // token row this lane addresses
       const int acol = lane >> 4;                           // +0 / +1 chunk

@@ -194,6 +194,15 @@ class Workload:
         v_cache[pb, :, po, :] = BF16_NAN
         return dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache)
 
+    def qk_norm_weights(self, l: int = 0):
+        """bf16 bits of the per-head RMSNorm weights of layer ``l`` for q and k:
+        [D] each, 1 + 0.25 * N(0, 1) (learned weights hover around one)."""
+        key = (self.seed, 1 + l, 5)
+        w = _normal_bf16(key, (2, self.spec.D))
+        x = bf16_bits_to_f32(w) * np.float32(0.25) + np.float32(1.0)
+        out = f32_to_bf16_bits(x)
+        return out[0], out[1]
+
     def poison_mask(self) -> np.ndarray:
         """bool [NB, BS]: slots holding no token before this step's append."""
         holds = np.zeros((self.NB, BLOCK_SIZE), dtype=bool)

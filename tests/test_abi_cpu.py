@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -164,3 +165,39 @@ def test_fused_entry_rejects_bad_new_rows(lib):
     assert call(good, _desc([2, 3, 64], BF16)) == -3
     assert call(_desc([3, 2, 64], BF16), _desc([3, 2, 64], BF16)) == -3
     assert call(_desc([2, 2, 64], BF16, data=8), good) == -5
+
+
+def test_rope_table_matches_its_definition(lib):
+    for theta, D, rows in [(1e6, 128, 300), (1e4, 64, 17), (10.0, 2, 5)]:
+        t = binding.forge_rope_cos_sin_table(theta, D, rows).numpy()
+        r = np.arange(rows, dtype=np.float64)[:, None]
+        a = r * theta ** (-2.0 * np.arange(D // 2) / D)
+        np.testing.assert_array_equal(t[:, : D // 2], np.cos(a).astype(np.float32))
+        np.testing.assert_array_equal(t[:, D // 2:], np.sin(a).astype(np.float32))
+    with pytest.raises(binding.ForgeError):
+        binding.forge_rope_cos_sin_table(1e4, 63, 4)
+
+
+def test_qk_options_are_validated(lib):
+    a = _decode_args()
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    kn = _desc([2, 2, 64], BF16)
+
+    def call(**kw):
+        o = binding.ForgeQKOptions()
+        o.norm_eps = kw.get("eps", 1e-6)
+        for name in ("q_norm_weight", "k_norm_weight", "rope_cos_sin"):
+            if name in kw:
+                setattr(o, name, ctypes.pointer(kw[name]))
+        return lib.forge_paged_qk_append_gqa_decode(r(a["q"]), r(kn), r(kn), ctypes.byref(o), r(a["k"]), r(a["v"]),
+                                                    r(a["bt"]), r(a["cl"]), a["scale"], r(a["out"]), None)
+    assert call(q_norm_weight=_desc([64], F32)) == -2
+    assert call(k_norm_weight=_desc([32], BF16)) == -3
+    assert call(q_norm_weight=_desc([64], BF16), eps=float("nan")) == -8
+    assert call(rope_cos_sin=_desc([10, 64], BF16)) == -2
+    assert call(rope_cos_sin=_desc([10, 32], F32)) == -3
+    assert call(rope_cos_sin=_desc([10, 64], F32, stride=[128, 1])) == -3
+    expect = -6 if not torch.cuda.is_available() else None
+    if expect is not None:   # valid options reach CUDA (absent here)
+        assert call(q_norm_weight=_desc([64], BF16), k_norm_weight=_desc([64], BF16),
+                    rope_cos_sin=_desc([10, 64], F32)) == -6
