@@ -5,8 +5,9 @@ A step is the whole hot path over one batch: the scatter of this step's new
 K/V token of every sequence into its cache slot and the paged GQA decode.
 By default a step is one forge_paged_append_gqa_decode launch per layer
 (append fused into the decode kernel); --path separate times
-forge_paged_kv_append followed by forge_paged_gqa_decode, and every run
-reports the other path too.  The default workload
+forge_paged_kv_append followed by forge_paged_gqa_decode, --path qk the
+fused call with RMSNorm + RoPE on q and the new k, and every run reports
+the other paths too.  The default workload
 is the Qwen3-4B-shaped attention layer: batch 32, context lengths uniform in
 [512, 8192], 32 query / 8 KV heads, head_dim 128, 16-token blocks, 10 % free
 blocks interleaved in the pool, bf16 storage.
@@ -40,6 +41,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged-GQA decode: KV-read HBM GB/s (% of GB300 peak) and µs per layer-step"
+PATH_NAMES = {
+    "fused": "forge_paged_append_gqa_decode: append + decode in one launch per layer",
+    "separate": "forge_paged_kv_append then forge_paged_gqa_decode, per layer",
+    "qk": "forge_paged_qk_append_gqa_decode: RMSNorm + RoPE on q/k, append and decode in one launch per layer",
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -331,6 +337,20 @@ def run_native(args, wl, out_bytes):
                                               pool_v[layer], d["tables"], d["lens"], wl.scale, out[layer],
                                               stream=stream)
 
+    # the q/k path (per-head RMSNorm + RoPE on q and the new k) in the same launch
+    qw, kw = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for a in wl.qk_norm_weights(0))
+    rope_table = binding.forge_rope_cos_sin_table(1e6, wl.D, wl.MB * 16).to(dev)
+
+    def fused_qk(layer):
+        binding.forge_paged_qk_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer], pool_k[layer],
+                                                 pool_v[layer], d["tables"], d["lens"], wl.scale, out[layer],
+                                                 q_norm_weight=qw, k_norm_weight=kw, norm_eps=1e-6,
+                                                 rope_cos_sin=rope_table, stream=stream)
+
+    def step_qk():
+        for layer in range(L):
+            fused_qk(layer)
+
     def step_separate():  # the two entry points: append, then decode, per layer
         for layer in range(L):
             append(layer)
@@ -344,9 +364,11 @@ def run_native(args, wl, out_bytes):
         for layer in range(L):
             decode(layer)
 
-    step, other = (step_fused, step_separate) if args.path == "fused" else (step_separate, step_fused)
-    kernel_only = step_fused if args.path == "fused" else decode_only
-    launches_per_step = L if args.path == "fused" else 2 * L
+    paths = {"fused": step_fused, "separate": step_separate, "qk": step_qk}
+    step = paths[args.path]
+    others = {k: v for k, v in paths.items() if k != args.path}
+    kernel_only = decode_only if args.path == "separate" else step
+    launches_per_step = 2 * L if args.path == "separate" else L
 
     def e2e_step():
         for k in ("q", "k_new", "v_new", "slots", "tables", "lens"):
@@ -356,8 +378,8 @@ def run_native(args, wl, out_bytes):
 
     with torch.cuda.stream(stream):
         for _ in range(3):  # eager calls first: the decode sizes its workspace on this stream
-            step_separate()
-            step_fused()
+            for fn in paths.values():
+                fn()
     stream.synchronize()
     assert binding.forge_paged_get_device_error(stream) == 0
 
@@ -377,7 +399,8 @@ def run_native(args, wl, out_bytes):
                     fn()
         return g.replay
 
-    run_step, run_other, run_kernel = runner(step), runner(other), runner(kernel_only)
+    run_step, run_kernel = runner(step), runner(kernel_only)
+    run_others = {k: runner(v) for k, v in others.items()}
     reps = args.steps // chunk
 
     def timed(run, n, per_call_events=False):
@@ -393,7 +416,7 @@ def run_native(args, wl, out_bytes):
         torch.cuda.synchronize(dev)
         return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
 
-    for run in (run_step, run_other, run_kernel):
+    for run in (run_step, run_kernel, *run_others.values()):
         timed(run, max(3, args.warmup) // chunk + 1)
 
     # ---------------- timed region (device-resident inputs)
@@ -411,7 +434,7 @@ def run_native(args, wl, out_bytes):
     clocks = ClockSampler.summarize(rows, w0, w1) if sampler else None
 
     # ---------------- the other way of running the step, for comparison
-    ms_other = timed(run_other, reps)[0]
+    ms_others = {k: timed(r, reps)[0] for k, r in run_others.items()}
 
     # ---------------- the dominant kernel alone, same launch path, events on its stream
     dec_reps = max(1, min(reps, 2000 // chunk))
@@ -435,7 +458,10 @@ def run_native(args, wl, out_bytes):
     assert binding.forge_paged_get_device_error(stream) == 0
     assert torch.isfinite(host_out.float()).all()
 
-    ms_total, e2e_ms, ms_other = max_over_ranks([ms_total, e2e_ms, ms_other], dev)
+    names = sorted(ms_others)
+    maxed = max_over_ranks([ms_total, e2e_ms] + [ms_others[k] for k in names], dev)
+    ms_total, e2e_ms = maxed[0], maxed[1]
+    ms_others = dict(zip(names, maxed[2:]))
 
     if rank != 0:
         if ws > 1:
@@ -462,9 +488,9 @@ def run_native(args, wl, out_bytes):
                                     "layers": L, "bytes_per_step": bytes_step,
                                     "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged_gqa_decode_split_kernel with fused append (one launch per layer)"
-                                if args.path == "fused" else
-                                "paged_gqa_decode_split_kernel (one decode call; split merge inside)"),
+                     "kernel": ("paged_gqa_decode_split_kernel (one decode call; split merge inside)"
+                                if args.path == "separate" else
+                                "paged_gqa_decode_split_kernel with fused append (one launch per layer)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),
@@ -473,12 +499,11 @@ def run_native(args, wl, out_bytes):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / args.steps, 5)},
         "gpu_launches": launches_per_step * args.steps,
-        "path": ("forge_paged_append_gqa_decode: append + decode in one launch per layer" if args.path == "fused"
-                 else "forge_paged_kv_append then forge_paged_gqa_decode, per layer"),
-        "other_path": {"path": "separate append + decode calls" if args.path == "fused" else "fused call",
-                       "ms_per_step": round(ms_other / args.steps, 5),
-                       "us_per_layer_step": round(ms_other / args.steps * 1e3 / L, 2),
-                       "value": round(aggregate_gbs(ws, bytes_step, args.steps, ms_other), 2)},
+        "path": PATH_NAMES[args.path],
+        "other_paths": {k: {"path": PATH_NAMES[k], "ms_per_step": round(v / args.steps, 5),
+                            "us_per_layer_step": round(v / args.steps * 1e3 / L, 2),
+                            "value": round(aggregate_gbs(ws, bytes_step, args.steps, v), 2)}
+                        for k, v in ms_others.items()},
         "clocks": clocks,
     }
     if ws > 1:
@@ -494,8 +519,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="qwen3_4b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
-                    help="fused: forge_paged_append_gqa_decode; separate: append then decode")
+    ap.add_argument("--path", choices=["fused", "separate", "qk"], default="fused",
+                    help="fused: forge_paged_append_gqa_decode; separate: append then decode; "
+                         "qk: forge_paged_qk_append_gqa_decode with RMSNorm + RoPE")
     ap.add_argument("--no-graphs", dest="graphs", action="store_false",
                     help="time eager C-ABI calls instead of replaying captured steps")
     args = ap.parse_args(argv)
