@@ -282,3 +282,33 @@ def custom_spec(name="custom", **kw) -> Spec:
     base = dict(B=2, Hq=8, Hkv=2, D=64, out_dtype="f32", lens="fixed", fixed_lens=(1, 1), seed=7)
     base.update(kw)
     return Spec(name, **base)
+
+
+@dataclasses.dataclass
+class RequestStream:
+    """Requests for the continuous-batching step driver, in arrival order."""
+    seq_ids: np.ndarray   # int64 [n]
+    prompts: np.ndarray   # int32 [n] prompt tokens
+    max_new: np.ndarray   # int32 [n] decode steps
+    arrive: np.ndarray    # int32 [n] step before which the request is submitted (non-decreasing)
+
+    def arriving(self, step: int):
+        """(seq_id, prompt, max_new) of the requests submitted before ``step``."""
+        idx = np.nonzero(self.arrive == step)[0]
+        return [(int(self.seq_ids[i]), int(self.prompts[i]), int(self.max_new[i])) for i in idx]
+
+
+def request_stream(n: int, seed: int, prompt_median: float = 1024.0, prompt_sigma: float = 1.0,
+                   prompt_max: int = 16383, new_min: int = 1, new_max: int = 256,
+                   arrivals_per_step: float = 1.0) -> RequestStream:
+    """n seeded requests: prompt lengths round(exp(N(ln median, sigma))) clipped
+    to [0, prompt_max], decode lengths uniform in [new_min, new_max], arrival
+    steps from exponential gaps of mean 1/arrivals_per_step steps (several
+    requests can arrive before the same step)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0x5e7]))
+    prompts = np.clip(np.rint(np.exp(rng.normal(math.log(prompt_median), prompt_sigma, n))), 0, prompt_max)
+    max_new = rng.integers(new_min, new_max, size=n, endpoint=True)
+    gaps = rng.exponential(1.0 / arrivals_per_step, n)
+    arrive = np.floor(np.cumsum(gaps) - gaps[0]).astype(np.int32)
+    ids = np.arange(n, dtype=np.int64) * 7 + 1000   # not the row numbers: ids are opaque
+    return RequestStream(ids, prompts.astype(np.int32), max_new.astype(np.int32), arrive)
