@@ -77,7 +77,8 @@ typedef enum {
     FORGE_ERR_ALIGN = -5,       /* a data pointer or stride breaks 16-byte alignment */
     FORGE_ERR_CUDA = -6,        /* a CUDA runtime call or a launch failed */
     FORGE_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than required */
-    FORGE_ERR_VALUE = -8        /* a scalar argument is out of range (e.g. non-finite scale) */
+    FORGE_ERR_VALUE = -8,       /* a scalar argument is out of range (e.g. non-finite scale) */
+    FORGE_ERR_CAPACITY = -9     /* a KV block pool or a decode batch has no room (forge_serving.h) */
 } forge_status;
 
 /* Device-side error codes (forge_paged_get_device_error). */

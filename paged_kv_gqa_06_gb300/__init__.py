@@ -7,7 +7,10 @@ Two operations, implemented as hand-written CUDA kernels behind a C ABI
     its slot of the paged block pool;
   * ``forge_paged_gqa_decode`` -- grouped-query attention of one new query
     token per sequence over that sequence's cached K/V, read through its
-    block table, with split-K partials merged by a reduce kernel.
+    block table, with split-K partials merged by a reduce kernel;
+  * ``forge_kv_pool_*`` / ``forge_batch_*`` (``include/forge_serving.h``) --
+    the KV block pool and the continuous-batching step driver that produce
+    the block tables, context lengths and slot mapping those calls read.
 
 The Python functions of the same names (``paged_kv_gqa_06_gb300.binding``)
 only marshal torch tensors into the C descriptors.  The CUDA library is
@@ -26,6 +29,21 @@ __all__ = [
     "forge_paged_gqa_decode_noalloc",
     "forge_paged_gqa_decode_workspace_bytes",
     "forge_paged_get_device_error",
+    "forge_kv_pool_create",
+    "forge_kv_pool_destroy",
+    "forge_kv_pool_add",
+    "forge_kv_pool_grow",
+    "forge_kv_pool_release",
+    "forge_kv_pool_free_blocks",
+    "forge_kv_pool_used_blocks",
+    "forge_kv_pool_sequence",
+    "forge_batch_create",
+    "forge_batch_destroy",
+    "forge_batch_submit",
+    "forge_batch_step",
+    "forge_batch_rows",
+    "forge_batch_events",
+    "forge_batch_apply",
 ]
 
 

@@ -13,6 +13,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -25,7 +26,7 @@ _DTYPES = {torch.bfloat16: FORGE_BF16, torch.float32: FORGE_F32,
 FORGE_OK = 0
 STATUS_NAMES = {0: "FORGE_OK", -1: "FORGE_ERR_NULL", -2: "FORGE_ERR_DTYPE", -3: "FORGE_ERR_SHAPE",
                 -4: "FORGE_ERR_UNSUPPORTED", -5: "FORGE_ERR_ALIGN", -6: "FORGE_ERR_CUDA",
-                -7: "FORGE_ERR_WORKSPACE", -8: "FORGE_ERR_VALUE"}
+                -7: "FORGE_ERR_WORKSPACE", -8: "FORGE_ERR_VALUE", -9: "FORGE_ERR_CAPACITY"}
 DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "context length longer than the table row",
                  3: "slot outside the pool", 4: "pipeline wait timed out", 5: "position beyond the rotary table"}
 
@@ -38,6 +39,12 @@ class ForgeTensor(ctypes.Structure):
 class ForgeQKOptions(ctypes.Structure):
     _fields_ = [("q_norm_weight", ctypes.POINTER(ForgeTensor)), ("k_norm_weight", ctypes.POINTER(ForgeTensor)),
                 ("norm_eps", ctypes.c_float), ("rope_cos_sin", ctypes.POINTER(ForgeTensor))]
+
+
+class ForgeBatchReport(ctypes.Structure):
+    _fields_ = [("running", ctypes.c_int32), ("waiting", ctypes.c_int32), ("admitted", ctypes.c_int32),
+                ("retired", ctypes.c_int32), ("preempted", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+                ("tokens", ctypes.c_int64)]
 
 
 class ForgeError(RuntimeError):
@@ -88,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_paged_get_device_error.restype = ctypes.c_int
         lib.forge_paged_version.argtypes = []
         lib.forge_paged_version.restype = ctypes.c_char_p
+        _type_serving(lib)
         _lib = lib
         return lib
 
@@ -241,3 +249,136 @@ def forge_paged_get_device_error(stream=None) -> int:
     rc = load_library().forge_paged_get_device_error(_stream_ptr(stream), ctypes.byref(code))
     _raise(rc, "forge_paged_get_device_error")
     return code.value
+
+
+# ---------------------------------------------------------------- KV block pool and batch driver
+# (include/forge_serving.h).  Handles are opaque pointers (Python ints); the
+# caller destroys what it creates.
+
+FORGE_BATCH_ADMITTED, FORGE_BATCH_RETIRED, FORGE_BATCH_PREEMPTED = 0, 1, 2
+
+
+def _type_serving(lib):
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    pi32, pi64 = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    T = ctypes.POINTER(ForgeTensor)
+    sig = {
+        "forge_kv_pool_create": ([i32, i32, i32], P),
+        "forge_kv_pool_destroy": ([P], None),
+        "forge_kv_pool_add": ([P, i64, i32], ctypes.c_int),
+        "forge_kv_pool_grow": ([P, i64, pi64], ctypes.c_int),
+        "forge_kv_pool_release": ([P, i64], ctypes.c_int),
+        "forge_kv_pool_free_blocks": ([P], i32),
+        "forge_kv_pool_used_blocks": ([P], i32),
+        "forge_kv_pool_sequence": ([P, i64, pi32, pi32, i32, pi32], ctypes.c_int),
+        "forge_batch_create": ([P, i32, i32], P),
+        "forge_batch_destroy": ([P], None),
+        "forge_batch_submit": ([P, i64, i32, i32], ctypes.c_int),
+        "forge_batch_step": ([P, ctypes.POINTER(ForgeBatchReport)], ctypes.c_int),
+        "forge_batch_rows": ([P, pi64, pi32, pi64, pi32], ctypes.c_int),
+        "forge_batch_events": ([P, ctypes.c_int, i32, pi64, pi32, pi32], ctypes.c_int),
+        "forge_batch_apply": ([P, T, T, T, P], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+
+
+def _np_ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def forge_kv_pool_create(num_blocks: int, block_size: int, max_blocks_per_seq: int) -> int:
+    h = load_library().forge_kv_pool_create(num_blocks, block_size, max_blocks_per_seq)
+    if not h:
+        raise ValueError("forge_kv_pool_create: bad sizes or out of memory")
+    return h
+
+
+def forge_kv_pool_destroy(pool: int) -> None:
+    load_library().forge_kv_pool_destroy(pool)
+
+
+def forge_kv_pool_add(pool: int, seq_id: int, num_tokens: int) -> None:
+    _raise(load_library().forge_kv_pool_add(pool, seq_id, num_tokens), "forge_kv_pool_add")
+
+
+def forge_kv_pool_grow(pool: int, seq_id: int) -> int:
+    """Add one token to seq_id; returns its cache slot."""
+    slot = ctypes.c_int64(-1)
+    _raise(load_library().forge_kv_pool_grow(pool, seq_id, ctypes.byref(slot)), "forge_kv_pool_grow")
+    return slot.value
+
+
+def forge_kv_pool_release(pool: int, seq_id: int) -> None:
+    _raise(load_library().forge_kv_pool_release(pool, seq_id), "forge_kv_pool_release")
+
+
+def forge_kv_pool_free_blocks(pool: int) -> int:
+    return load_library().forge_kv_pool_free_blocks(pool)
+
+
+def forge_kv_pool_used_blocks(pool: int) -> int:
+    return load_library().forge_kv_pool_used_blocks(pool)
+
+
+def forge_kv_pool_sequence(pool: int, seq_id: int):
+    """(token count, list of block ids) of seq_id."""
+    lib = load_library()
+    n, length = ctypes.c_int32(0), ctypes.c_int32(0)
+    _raise(lib.forge_kv_pool_sequence(pool, seq_id, ctypes.byref(length), None, 0, ctypes.byref(n)),
+           "forge_kv_pool_sequence")
+    blocks = np.zeros(max(1, n.value), dtype=np.int32)
+    _raise(lib.forge_kv_pool_sequence(pool, seq_id, None, _np_ptr(blocks, ctypes.c_int32), n.value, None),
+           "forge_kv_pool_sequence")
+    return length.value, blocks[: n.value].tolist()
+
+
+def forge_batch_create(pool: int, rows: int, token_budget: int) -> int:
+    h = load_library().forge_batch_create(pool, rows, token_budget)
+    if not h:
+        raise ValueError("forge_batch_create: bad arguments or out of memory")
+    return h
+
+
+def forge_batch_destroy(batch: int) -> None:
+    load_library().forge_batch_destroy(batch)
+
+
+def forge_batch_submit(batch: int, seq_id: int, prompt_tokens: int, max_new_tokens: int) -> None:
+    _raise(load_library().forge_batch_submit(batch, seq_id, prompt_tokens, max_new_tokens), "forge_batch_submit")
+
+
+def forge_batch_step(batch: int) -> dict:
+    """One host step; returns the forge_batch_report fields as a dict."""
+    rep = ForgeBatchReport()
+    _raise(load_library().forge_batch_step(batch, ctypes.byref(rep)), "forge_batch_step")
+    return {name: getattr(rep, name) for name, _ in ForgeBatchReport._fields_}
+
+
+def forge_batch_rows(batch: int, rows: int) -> dict:
+    """The last step's per-row state as numpy arrays of length ``rows``."""
+    out = {"seq_ids": np.zeros(rows, np.int64), "context_lens": np.zeros(rows, np.int32),
+           "slots": np.zeros(rows, np.int64), "new_blocks": np.zeros(rows, np.int32)}
+    _raise(load_library().forge_batch_rows(batch, _np_ptr(out["seq_ids"], ctypes.c_int64),
+                                           _np_ptr(out["context_lens"], ctypes.c_int32),
+                                           _np_ptr(out["slots"], ctypes.c_int64),
+                                           _np_ptr(out["new_blocks"], ctypes.c_int32)), "forge_batch_rows")
+    return out
+
+
+def forge_batch_events(batch: int, kind: int) -> list:
+    """The last step's events of one kind as (seq_id, row, tokens) tuples."""
+    lib = load_library()
+    n = lib.forge_batch_events(batch, kind, 0, None, None, None)
+    _raise(min(n, 0), "forge_batch_events")
+    seq, row, tok = np.zeros(max(1, n), np.int64), np.zeros(max(1, n), np.int32), np.zeros(max(1, n), np.int32)
+    lib.forge_batch_events(batch, kind, n, _np_ptr(seq, ctypes.c_int64), _np_ptr(row, ctypes.c_int32),
+                           _np_ptr(tok, ctypes.c_int32))
+    return [(int(seq[i]), int(row[i]), int(tok[i])) for i in range(n)]
+
+
+def forge_batch_apply(batch: int, block_tables, context_lens, slot_mapping, stream=None) -> None:
+    rc = load_library().forge_batch_apply(batch, _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                          _ref(describe(slot_mapping)), _stream_ptr(stream))
+    _raise(rc, "forge_batch_apply")

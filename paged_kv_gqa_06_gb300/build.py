@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libforge_paged.so")
-SOURCES = ["abi.cu", "append.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "append.cu", "decode.cu", "noalloc.cu", "serving.cu"]
 HEADERS = ["common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -36,7 +36,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    deps.append(os.path.join(ROOT, "include", "forge_paged.h"))
+    deps += [os.path.join(ROOT, "include", h) for h in ("forge_paged.h", "forge_serving.h")]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 

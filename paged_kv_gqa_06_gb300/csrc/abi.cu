@@ -545,6 +545,7 @@ const char* forge_status_string(int status) {
     case FORGE_ERR_CUDA: return "FORGE_ERR_CUDA: a CUDA call or launch failed";
     case FORGE_ERR_WORKSPACE: return "FORGE_ERR_WORKSPACE: workspace missing or too small";
     case FORGE_ERR_VALUE: return "FORGE_ERR_VALUE: scalar argument out of range";
+    case FORGE_ERR_CAPACITY: return "FORGE_ERR_CAPACITY: the block pool or the batch has no room";
     default: return "unknown forge status";
   }
 }

@@ -1,6 +1,6 @@
 """The C ABI on a machine without a GPU: the library loads, exports every
-entry point include/forge_paged.h declares, and rejects bad arguments on the
-host before touching CUDA."""
+entry point include/*.h declares, and rejects bad arguments on the host
+before touching CUDA."""
 import ctypes
 import os
 import re
@@ -12,7 +12,8 @@ import torch
 from paged_kv_gqa_06_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "forge_paged.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,19 +24,20 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"FORGE_API\s+[\w\s\*]*?\b(forge_\w+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
+    assert len(HEADERS) >= 2
     names = _declared_functions()
-    assert len(names) >= 7
+    assert len(names) >= 25 and "forge_batch_apply" in names and "forge_paged_gqa_decode" in names
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in forge_paged.h but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
 
 def test_status_strings_and_version(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert lib.forge_status_string(code)
     assert lib.forge_status_string(-99) == b"unknown forge status"
     assert lib.forge_paged_version() == b"0.1.0"
