@@ -1,4 +1,4 @@
-"""CPU oracle for paged-KV append and paged GQA decode.
+"""CPU oracle for paged-KV append, paged GQA decode and paged prefill.
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and
 ``bench.py``'s CPU-baseline / reference legs may import this package.  It
@@ -81,6 +81,9 @@ def _load():
             lib.oracle_rmsnorm.restype = None
             lib.oracle_rope.argtypes = [P, P, ctypes.c_double, i, i]
             lib.oracle_rope.restype = None
+            lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, ctypes.c_double, P,
+                                                 i, i, i, i, i, i, i, i]
+            lib.oracle_paged_prefill.restype = i
             _lib = lib
     return _lib
 
@@ -148,6 +151,39 @@ def paged_gqa_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
                                          float(scale), _ptr(out),
                                          B, Hq, Hkv, D, NB, BS, MB, int(nthreads))
     _check(rc, "decode")
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                  nthreads: int | None = None) -> np.ndarray:
+    """fp64 causal prefill over the paged cache; returns out [T, Hq, D] float64.
+
+    q: uint16 [T, Hq, D] packed by query_start (int32 [B+1], starting at 0);
+    sequence b's query tokens sit at the last n_b positions of its
+    context_lens[b] tokens.  Other arguments as in paged_gqa_decode.
+    """
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint16)
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    B = context_lens.shape[0]
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.ndim != 2 or block_tables.shape[0] != B or query_start.shape != (B + 1,):
+        raise ValueError("block_tables / query_start shape mismatch")
+    if B and int(query_start[-1]) != T:
+        raise ValueError("query_start[B] must equal the number of query tokens")
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    if nthreads is None:
+        nthreads = host_cores()
+    rc = _load().oracle_paged_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                      _ptr(context_lens), _ptr(query_start), float(scale), _ptr(out),
+                                      B, Hq, Hkv, D, NB, BS, block_tables.shape[1], int(nthreads))
+    _check(rc, "prefill")
     return out
 
 

@@ -1,5 +1,6 @@
 /*
- * CPU oracle for paged-KV append and paged grouped-query-attention decode.
+ * CPU oracle for paged-KV append, paged grouped-query-attention decode and
+ * paged prefill.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
  * calls this file: only the test suite, the smoke check and the benchmark's
@@ -250,6 +251,157 @@ int oracle_paged_gqa_decode(const uint16_t *q, const uint16_t *k_cache,
         ++started;
     }
     if (started == 0) decode_worker(&j);
+    for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
+    free(tids);
+    return j.status;
+}
+
+/*
+ * Paged prefill (causal attention of a chunk of new query tokens).
+ *
+ * "Make the Engine Talk", 1.2: the prefill runs one forward pass over all
+ * prompt tokens at once and fills the KV cache; forge-engine README, "What it
+ * implements": prefill and decode are separate engine paths over the same
+ * paged cache.  The chunk's K/V is already in the cache (written by the
+ * append), so for sequence b with n_b = query_start[b+1] - query_start[b]
+ * query tokens and context length L_b (the chunk included), query token i
+ * sits at position p = L_b - n_b + i and attends to positions t <= p:
+ *   out[query_start[b] + i, h, :] =
+ *       sum_{t <= p} softmax_t(scale * q . K_b[t]) V_b[t]
+ * with the same head grouping and cache addressing as the decode (which is
+ * the n_b = 1 case).  n_b = 0 produces nothing; n_b > L_b is an error.
+ */
+typedef struct {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens, *query_start;
+    double scale;
+    double *out;
+    int B, Hq, Hkv, D, NB, BS, MB;
+    int max_len;
+    int next_item; /* shared work counter over (b, h) */
+    int status;
+} prefill_job;
+
+/* All query tokens of one (sequence, query head). */
+static int prefill_one(const prefill_job *j, int b, int h, double *K, double *V, double *s) {
+    const int D = j->D, BS = j->BS, Hkv = j->Hkv;
+    const int G = j->Hq / j->Hkv;
+    const int g = h / G;
+    const int L = j->context_lens[b];
+    const int q0 = j->query_start[b];
+    const int n = j->query_start[b + 1] - q0;
+    if (n <= 0) return n == 0 ? ORACLE_OK : ORACLE_ERR_ARG;
+    if (n > L) return ORACLE_ERR_LEN;
+    if (L > j->MB * BS) return ORACLE_ERR_LEN;
+
+    /* gather the sequence's L tokens of KV head g into contiguous rows */
+    for (int t = 0; t < L; ++t) {
+        int32_t blk = j->block_tables[(size_t)b * j->MB + t / BS];
+        if (blk < 0 || blk >= j->NB) return ORACLE_ERR_BLOCK;
+        size_t row = (((size_t)blk * Hkv + g) * BS + (size_t)(t % BS)) * (size_t)D;
+        for (int d = 0; d < D; ++d) {
+            K[(size_t)t * D + d] = bf16_bits_to_double(j->k_cache[row + d]);
+            V[(size_t)t * D + d] = bf16_bits_to_double(j->v_cache[row + d]);
+        }
+    }
+
+    for (int i = 0; i < n; ++i) {
+        const int p = L - n + i; /* this query token's position */
+        const uint16_t *qrow = j->q + ((size_t)(q0 + i) * j->Hq + h) * (size_t)D;
+        double *o = j->out + ((size_t)(q0 + i) * j->Hq + h) * (size_t)D;
+        double m = -INFINITY;
+        for (int t = 0; t <= p; ++t) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += bf16_bits_to_double(qrow[d]) * K[(size_t)t * D + d];
+            s[t] = j->scale * acc;
+            if (s[t] > m) m = s[t];
+        }
+        double den = 0.0;
+        for (int t = 0; t <= p; ++t) {
+            s[t] = exp(s[t] - m);
+            den += s[t];
+        }
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int t = 0; t <= p; ++t)
+            for (int d = 0; d < D; ++d) o[d] += s[t] * V[(size_t)t * D + d];
+        for (int d = 0; d < D; ++d) o[d] /= den;
+    }
+    return ORACLE_OK;
+}
+
+static void *prefill_worker(void *arg) {
+    prefill_job *j = (prefill_job *)arg;
+    size_t n = (size_t)(j->max_len > 0 ? j->max_len : 1);
+    double *K = (double *)malloc(n * (size_t)j->D * sizeof(double));
+    double *V = (double *)malloc(n * (size_t)j->D * sizeof(double));
+    double *s = (double *)malloc(n * sizeof(double));
+    if (!K || !V || !s) {
+        __atomic_store_n(&j->status, ORACLE_ERR_NOMEM, __ATOMIC_RELAXED);
+    } else {
+        const int items = j->B * j->Hq;
+        for (;;) {
+            int it = __atomic_fetch_add(&j->next_item, 1, __ATOMIC_RELAXED);
+            if (it >= items) break;
+            int rc = prefill_one(j, it / j->Hq, it % j->Hq, K, V, s);
+            if (rc != ORACLE_OK) __atomic_store_n(&j->status, rc, __ATOMIC_RELAXED);
+        }
+    }
+    free(K);
+    free(V);
+    free(s);
+    return NULL;
+}
+
+/*
+ * Prefill for every sequence.  q and out are packed by query_start ([B+1],
+ * query_start[0] = 0, non-decreasing): q [T, Hq, D] bf16 bits, out [T, Hq, D]
+ * fp64 with T = query_start[B].  Other layouts as in the decode.  nthreads as
+ * in the decode.
+ */
+int oracle_paged_prefill(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         const int32_t *query_start, double scale, double *out, int B, int Hq,
+                         int Hkv, int D, int NB, int BS, int MB, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || BS <= 0 || MB < 0 || NB < 0)
+        return ORACLE_ERR_ARG;
+    if (B > 0 && query_start[0] != 0) return ORACLE_ERR_ARG;
+    for (int b = 0; b < B; ++b)
+        if (query_start[b + 1] < query_start[b]) return ORACLE_ERR_ARG;
+    prefill_job j;
+    j.q = q;
+    j.k_cache = k_cache;
+    j.v_cache = v_cache;
+    j.block_tables = block_tables;
+    j.context_lens = context_lens;
+    j.query_start = query_start;
+    j.scale = scale;
+    j.out = out;
+    j.B = B;
+    j.Hq = Hq;
+    j.Hkv = Hkv;
+    j.D = D;
+    j.NB = NB;
+    j.BS = BS;
+    j.MB = MB;
+    j.next_item = 0;
+    j.status = ORACLE_OK;
+    j.max_len = 0;
+    for (int b = 0; b < B; ++b)
+        if (context_lens[b] > j.max_len) j.max_len = context_lens[b];
+    if (j.max_len > MB * BS) return ORACLE_ERR_LEN;
+
+    if (nthreads <= 1) {
+        prefill_worker(&j);
+        return j.status;
+    }
+    pthread_t *tids = (pthread_t *)malloc((size_t)nthreads * sizeof(pthread_t));
+    if (!tids) return ORACLE_ERR_NOMEM;
+    int started = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        if (pthread_create(&tids[i], NULL, prefill_worker, &j) != 0) break;
+        ++started;
+    }
+    if (started == 0) prefill_worker(&j);
     for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
     free(tids);
     return j.status;

@@ -112,6 +112,7 @@ class Spec:
     nb_fixed: int = 0         # pool size when fixed by the recipe
     layers: int = 1
     seed: int = 0
+    chunk: int = 0            # prefill: new tokens per sequence (0 = the whole context)
     description: str = ""
 
 
@@ -137,6 +138,15 @@ SPECS = {
         "skewed_bf16", B=4, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="fixed",
         fixed_lens=(32768, 1024, 256, 17), seed=1004,
         description="skewed long context, bf16 out"),
+    "prefill_tiny": Spec(
+        "prefill_tiny", B=4, Hq=8, Hkv=2, D=64, out_dtype="f32", lens="fixed",
+        fixed_lens=(20, 45, 7, 64), chunk=24, free_frac=0.2, seed=1011,
+        description="prefill: batch 4, lens {20,45,7,64}, last min(24, L) tokens new, 8/2 heads, D 64, fp32"),
+    "prefill_4b": Spec(
+        "prefill_4b", B=8, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="uniform",
+        lo=512, hi=4096, chunk=512, k_mul=2.0, free_frac=0.10, seed=1012,
+        description="Qwen3-4B-shaped chunked prefill: batch 8, a 512-token chunk ending contexts U[512,4096], "
+                    "32/8 heads, D 128, 10% free blocks, K x2, bf16 out"),
     "cb36": Spec(
         "cb36", B=64, Hq=32, Hkv=8, D=128, out_dtype="bf16", lens="lognormal",
         lo=1, hi=16384, median=1024.0, sigma=1.0, layers=36, seed=1005,
@@ -203,11 +213,13 @@ class Workload:
         out = f32_to_bf16_bits(x)
         return out[0], out[1]
 
-    def poison_mask(self) -> np.ndarray:
-        """bool [NB, BS]: slots holding no token before this step's append."""
+    def poison_mask(self, new_tokens=None) -> np.ndarray:
+        """bool [NB, BS]: slots holding no token before this step's append
+        (of one token per sequence, or of ``new_tokens[b]``)."""
         holds = np.zeros((self.NB, BLOCK_SIZE), dtype=bool)
         for b in range(self.B):
-            n_before = int(self.context_lens[b]) - 1   # tokens already cached
+            n_new = 1 if new_tokens is None else int(new_tokens[b])
+            n_before = int(self.context_lens[b]) - n_new   # tokens already cached
             for j in range(-(-n_before // BLOCK_SIZE) if n_before > 0 else 0):
                 p = int(self.block_tables[b, j])
                 cnt = min(BLOCK_SIZE, n_before - j * BLOCK_SIZE)
@@ -312,3 +324,69 @@ def request_stream(n: int, seed: int, prompt_median: float = 1024.0, prompt_sigm
     arrive = np.floor(np.cumsum(gaps) - gaps[0]).astype(np.int32)
     ids = np.arange(n, dtype=np.int64) * 7 + 1000   # not the row numbers: ids are opaque
     return RequestStream(ids, prompts.astype(np.int32), max_new.astype(np.int32), arrive)
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    """A chunked-prefill batch over the same paged layout: sequence b ends with
+    n_b = chunk_lens[b] new tokens at positions L_b - n_b .. L_b - 1, packed in
+    ``query_start`` order.  Their K/V go into the cache one slot per token
+    (``slot_mapping``, int64 [T]) before the prefill attends over all L_b
+    tokens; every slot that holds no token before that append is NaN."""
+    base: Workload
+    chunk_lens: np.ndarray    # int32 [B]
+    query_start: np.ndarray   # int32 [B + 1]
+    slot_mapping: np.ndarray  # int64 [T]
+
+    def __getattr__(self, name):          # shapes, tables, lens and scale come from the base batch
+        if name == "base":
+            raise AttributeError(name)
+        return getattr(self.base, name)
+
+    @property
+    def T(self): return int(self.query_start[-1])
+
+    def layer(self, l: int = 0) -> dict:
+        """q [T,Hq,D], the chunk's k/v [T,Hkv,D] and the pre-append caches of layer ``l``."""
+        s = self.base.spec
+        key = (self.base.seed, 1 + l)
+        q = _normal_bf16((*key, 10), (self.T, s.Hq, s.D))
+        k_new = _normal_bf16((*key, 11), (self.T, s.Hkv, s.D), s.k_mul)
+        v_new = _normal_bf16((*key, 12), (self.T, s.Hkv, s.D))
+        shape = (self.base.NB, s.Hkv, BLOCK_SIZE, s.D)
+        k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
+        v_cache = _normal_bf16((*key, 4), shape)
+        pb, po = np.nonzero(self.base.poison_mask(self.chunk_lens))
+        k_cache[pb, :, po, :] = BF16_NAN
+        v_cache[pb, :, po, :] = BF16_NAN
+        return dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache)
+
+    def attended_pairs(self) -> int:
+        """(query token, cached token) pairs the causal prefill visits: sum over
+        sequences and query tokens of position + 1.  (Accounting only.)"""
+        n = self.chunk_lens.astype(np.int64)
+        L = self.base.context_lens.astype(np.int64)
+        return int(np.sum(n * (L - n) + n * (n + 1) // 2))
+
+
+def make_prefill(name_or_spec, seed: int | None = None, context_lens=None, chunk_lens=None) -> PrefillWorkload:
+    """A prefill batch: tables and lengths as ``make_workload`` builds them,
+    n_b = min(chunk, L_b) new tokens per sequence (all L_b when the spec's
+    chunk is 0) unless ``chunk_lens`` gives them."""
+    base = make_workload(name_or_spec, seed, context_lens)
+    L = base.context_lens
+    if chunk_lens is None:
+        n = np.minimum(L, base.spec.chunk) if base.spec.chunk > 0 else L.copy()
+    else:
+        n = np.asarray(chunk_lens, dtype=np.int32)
+        if n.shape != L.shape or np.any(n < 0) or np.any(n > L):
+            raise ValueError("chunk_lens must satisfy 0 <= n_b <= context_lens[b]")
+    n = n.astype(np.int32)
+    qs = np.zeros(base.B + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(n)
+    slots = np.empty(int(qs[-1]), dtype=np.int64)
+    for b in range(base.B):
+        for i in range(int(n[b])):
+            t = int(L[b]) - int(n[b]) + i
+            slots[qs[b] + i] = int(base.block_tables[b, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE
+    return PrefillWorkload(base=base, chunk_lens=n, query_start=qs, slot_mapping=slots)
