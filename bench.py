@@ -660,6 +660,108 @@ def run_serving(args, wl):
     }
 
 
+def run_prefill(args, name):
+    """Paged prefill: the run's K/V appended (forge_paged_kv_append, one slot
+    per token), then forge_paged_prefill over the batch.  A contraction, so
+    the roofline is the tensor peak: algorithmic FLOPs are 4 * D per (query
+    token, attended token, query head) -- QK^T and PV, causal pairs only."""
+    import torch
+
+    from paged_kv_gqa_06_gb300 import binding as B
+    from paged_kv_gqa_06_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B.load_library()
+    pw = W.make_prefill(name)
+    t = pw.layer(0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    copies = 4                                   # rotate cache copies so the K/V do not sit in L2
+    kc = [bf(t["k_cache"]) for _ in range(copies)]
+    vc = [bf(t["v_cache"]) for _ in range(copies)]
+    q, k_new, v_new = bf(t["q"]), bf(t["k_new"]), bf(t["v_new"])
+    slots = torch.from_numpy(pw.slot_mapping).to(dev)
+    tables = torch.from_numpy(pw.block_tables).to(dev)
+    lens = torch.from_numpy(pw.context_lens).to(dev)
+    qs = torch.from_numpy(pw.query_start).to(dev)
+    out_dt = torch.bfloat16 if pw.spec.out_dtype == "bf16" else torch.float32
+    out = torch.empty(pw.T, pw.Hq, pw.D, dtype=out_dt, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(c, with_append=True):
+        if with_append:
+            B.forge_paged_kv_append(k_new, v_new, slots, kc[c], vc[c], stream=stream)
+        B.forge_paged_prefill(q, kc[c], vc[c], tables, lens, qs, pw.scale, out, stream=stream)
+
+    graphs = {}
+    for key in (True, False):
+        with torch.cuda.stream(stream):
+            for c in range(copies):
+                step(c, key)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in range(copies):
+                step(c, key)
+        graphs[key] = g
+    reps = max(1, args.steps // copies)
+
+    def timed(g, n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(n):
+                g.replay()
+            ev1.record(stream)
+        stream.synchronize()
+        return ev0.elapsed_time(ev1) / (n * copies)
+
+    for g in graphs.values():
+        timed(g, max(1, args.warmup // copies + 1))
+    sampler = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+    time.sleep(0.3)
+    w0 = time.time()
+    ms_step = timed(graphs[True], reps)
+    ms_kernel = timed(graphs[False], reps)
+    w1 = time.time()
+    clocks = ClockSampler.summarize(sampler.stop(), w0, w1)
+    assert B.forge_paged_get_device_error(stream) == 0
+    assert torch.isfinite(out.float()).all()
+
+    pairs = pw.attended_pairs()
+    flops = 4.0 * pw.D * pw.Hq * pairs
+    kv_bytes = int(pw.context_lens.astype(np.int64).sum()) * pw.Hkv * pw.D * 2 * 2
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            peak, peak_src = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, " \
+                                                                 "cuBLAS bf16 GEMM burst), of measured"
+    else:
+        peak, peak_src = 1900.0, "fallback (1.9 PFLOP/s bf16 burst), of fallback"
+    tflops_kernel = flops / (ms_kernel * 1e-3) / 1e12
+    tflops_step = flops / (ms_step * 1e-3) / 1e12
+    return {
+        "metric": "paged prefill: attention TFLOP/s (causal pairs only) and us per call",
+        "value": round(tflops_step, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": reps * copies,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: {pw.spec.description}", "batch": pw.B, "query_tokens": pw.T,
+                   "context_tokens": int(pw.context_lens.sum()), "attended_pairs": pairs,
+                   "flops_rule": "4 * D * Hq per (query token, attended token)",
+                   "step": "forge_paged_kv_append of the run's K/V + forge_paged_prefill, CUDA graph",
+                   "l2": f"{copies} cache copies rotated ({copies * kv_bytes / 1e6:.0f} MB of K/V vs 126 MB L2)"},
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)",
+                     "achieved": round(tflops_kernel, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops_kernel / peak, 4), "traffic": None,
+                     "prefill_us": round(ms_kernel * 1e3, 2), "peak_source": peak_src},
+        "gpu_launches": 2 * reps * copies,
+        "clocks": clocks,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -673,6 +775,8 @@ def main(argv=None):
                          "qk: forge_paged_qk_append_gqa_decode with RMSNorm + RoPE")
     ap.add_argument("--no-graphs", dest="graphs", action="store_false",
                     help="time eager C-ABI calls instead of replaying captured steps")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the paged prefill on a prefill workload (default prefill_4b)")
     ap.add_argument("--serving", action="store_true",
                     help="continuous batching through the block pool + batch driver (multi-layer workloads)")
     args = ap.parse_args(argv)
@@ -680,6 +784,12 @@ def main(argv=None):
         args.warmup = 3
 
     from paged_kv_gqa_06_gb300 import workloads as W
+    if args.prefill:
+        import __graft_entry__
+        __graft_entry__.build()
+        name = args.workload if args.workload.startswith("prefill") else "prefill_4b"
+        print(json.dumps(run_prefill(args, name)), flush=True)
+        return 0
     wl = W.make_workload(args.workload)
     out_bytes = 4 if wl.spec.out_dtype == "f32" else 2
 

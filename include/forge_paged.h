@@ -88,6 +88,7 @@ typedef enum {
 #define FORGE_DEVERR_SLOT 3       /* slot_mapping[b] >= NB * BS */
 #define FORGE_DEVERR_TIMEOUT 4    /* a pipeline wait gave up (should never happen) */
 #define FORGE_DEVERR_POSITION 5   /* context_lens[b] - 1 beyond the rotary table (rotation skipped) */
+#define FORGE_DEVERR_QUERY 6      /* prefill: query_start not 0 at b = 0, decreasing, past T, or n_b > L_b */
 
 /*
  * forge_paged_kv_append -- write this step's new K/V token of every sequence
@@ -287,6 +288,41 @@ FORGE_API int forge_paged_gqa_decode_noalloc(const forge_tensor *q, const forge_
                                    void *stream);
 
 /* Human-readable name of a forge_status.  Never NULL. */
+/*
+ * forge_paged_prefill -- causal attention of a run of new query tokens per
+ * sequence over its paged cache ("Make the Engine Talk", 1.2: the prefill
+ * runs one forward pass over all of a prompt's tokens at once and fills the
+ * cache; chunked, the run is the next piece of a longer context).  The run's
+ * K/V must already be in the cache (forge_paged_kv_append with one slot per
+ * token).  For sequence b with n_b = query_start[b+1] - query_start[b] query
+ * tokens and L_b = context_lens[b] cached tokens (the run included), query
+ * row query_start[b] + i sits at position p = L_b - n_b + i and
+ *   out[row, h, :] = sum_{t <= p} softmax_t(scale * q[row, h, :] . K_b[t, h/G, :]) V_b[t, h/G, :]
+ * with K_b / V_b addressed through block_tables as in the decode (which is
+ * the n_b = 1 case).
+ *
+ *   q             bf16 [T, Hq, D]; last dim contiguous, 16-byte aligned, other
+ *                 strides multiples of 8 elements.
+ *   k_cache,
+ *   v_cache       bf16 [NB, Hkv, 16, D] (as for the decode).
+ *   block_tables  int32 [B, MB], inner stride 1.
+ *   context_lens  int32 [B], contiguous: L_b, at most MB * 16.
+ *   query_start   int32 [B + 1], contiguous: 0 = query_start[0] <= ... <=
+ *                 query_start[B] <= T; 0 <= n_b <= L_b.
+ *   scale         finite.
+ *   out           f32 or bf16 [T, Hq, D], strides as q; rows outside every
+ *                 sequence's range are left as they are.
+ * D in {64, 128}, Hq / Hkv in {1, 2, 4, 8}.  Enqueues one kernel on `stream`
+ * and returns without syncing; no allocation, capturable.  A query_start or
+ * length that breaks the rules above is recorded as FORGE_DEVERR_QUERY /
+ * FORGE_DEVERR_LENGTH and that sequence's rows are not written; a bad block
+ * id as FORGE_DEVERR_BLOCK_ID.
+ */
+FORGE_API int forge_paged_prefill(const forge_tensor *q, const forge_tensor *k_cache,
+                                  const forge_tensor *v_cache, const forge_tensor *block_tables,
+                                  const forge_tensor *context_lens, const forge_tensor *query_start,
+                                  float scale, forge_tensor *out, void *stream);
+
 FORGE_API const char *forge_status_string(int status);
 
 /*

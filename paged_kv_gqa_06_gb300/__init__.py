@@ -8,6 +8,8 @@ Two operations, implemented as hand-written CUDA kernels behind a C ABI
   * ``forge_paged_gqa_decode`` -- grouped-query attention of one new query
     token per sequence over that sequence's cached K/V, read through its
     block table, with split-K partials merged by a reduce kernel;
+  * ``forge_paged_prefill`` -- causal attention of a run of new query tokens
+    per sequence (a prompt, or the next chunk of one) over the paged cache;
   * ``forge_kv_pool_*`` / ``forge_batch_*`` (``include/forge_serving.h``) --
     the KV block pool and the continuous-batching step driver that produce
     the block tables, context lengths and slot mapping those calls read.
@@ -27,6 +29,7 @@ __all__ = [
     "forge_rope_cos_sin_table",
     "forge_paged_gqa_decode_ex",
     "forge_paged_gqa_decode_noalloc",
+    "forge_paged_prefill",
     "forge_paged_gqa_decode_workspace_bytes",
     "forge_paged_get_device_error",
     "forge_kv_pool_create",

@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "FORGE_OK", -1: "FORGE_ERR_NULL", -2: "FORGE_ERR_DTYPE", -3: 
                 -4: "FORGE_ERR_UNSUPPORTED", -5: "FORGE_ERR_ALIGN", -6: "FORGE_ERR_CUDA",
                 -7: "FORGE_ERR_WORKSPACE", -8: "FORGE_ERR_VALUE", -9: "FORGE_ERR_CAPACITY"}
 DEVICE_ERRORS = {0: "none", 1: "block id outside the pool", 2: "context length longer than the table row",
-                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "position beyond the rotary table"}
+                 3: "slot outside the pool", 4: "pipeline wait timed out", 5: "position beyond the rotary table",
+                 6: "prefill query_start out of order or longer than the context"}
 
 
 class ForgeTensor(ctypes.Structure):
@@ -85,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_rope_cos_sin_table.restype = ctypes.c_int
         lib.forge_paged_append_gqa_decode.argtypes = [T, T, T, T, T, T, T, ctypes.c_float, T, P]
         lib.forge_paged_append_gqa_decode.restype = ctypes.c_int
+        lib.forge_paged_prefill.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, P]
+        lib.forge_paged_prefill.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_noalloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, P]
         lib.forge_paged_gqa_decode_noalloc.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
@@ -211,6 +214,16 @@ def forge_rope_cos_sin_table(theta: float, D: int, rows: int) -> torch.Tensor:
                                                  ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_float)))
     _raise(rc, "forge_rope_cos_sin_table")
     return t
+
+
+def forge_paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, out, stream=None):
+    """Causal prefill of the query rows packed by ``query_start`` into ``out``; returns ``out``."""
+    lib = load_library()
+    rc = lib.forge_paged_prefill(_ref(describe(q)), _ref(describe(k_cache)), _ref(describe(v_cache)),
+                                 _ref(describe(block_tables)), _ref(describe(context_lens)),
+                                 _ref(describe(query_start)), float(scale), _ref(describe(out)), _stream_ptr(stream))
+    _raise(rc, "forge_paged_prefill")
+    return out
 
 
 def forge_paged_gqa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):

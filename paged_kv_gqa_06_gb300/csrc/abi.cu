@@ -534,6 +534,75 @@ int append_decode_impl(const forge_tensor* q, const forge_tensor* k_new, const f
 
 extern "C" {
 
+int forge_paged_prefill(const forge_tensor* q, const forge_tensor* k_cache, const forge_tensor* v_cache,
+                        const forge_tensor* block_tables, const forge_tensor* context_lens,
+                        const forge_tensor* query_start, float scale, forge_tensor* out, void* stream) {
+  FORGE_TRY(check_tensor(q, FORGE_BF16, 3));
+  FORGE_TRY(check_cache(k_cache));
+  FORGE_TRY(check_cache(v_cache));
+  FORGE_TRY(check_tensor(block_tables, FORGE_I32, 2));
+  FORGE_TRY(check_tensor(context_lens, FORGE_I32, 1));
+  FORGE_TRY(check_tensor(query_start, FORGE_I32, 1));
+  if (!out) return FORGE_ERR_NULL;
+  if (out->dtype != FORGE_BF16 && out->dtype != FORGE_F32) return FORGE_ERR_DTYPE;
+  if (out->ndim != 3) return FORGE_ERR_SHAPE;
+  const int64_t T = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t NB = k_cache->shape[0], Hkv = k_cache->shape[1];
+  const int64_t B = context_lens->shape[0], MB = block_tables->shape[1];
+  for (int i = 0; i < 4; ++i)
+    if (v_cache->shape[i] != k_cache->shape[i]) return FORGE_ERR_SHAPE;
+  if (k_cache->shape[3] != D) return FORGE_ERR_SHAPE;
+  if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != D) return FORGE_ERR_SHAPE;
+  if (block_tables->shape[0] != B || query_start->shape[0] != B + 1) return FORGE_ERR_SHAPE;
+  if (T > INT32_MAX / 2 || B > INT32_MAX / 2 || Hkv > 65535 || NB > INT32_MAX || MB > (INT32_MAX / kBlockSize))
+    return FORGE_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FORGE_ERR_UNSUPPORTED;
+  if (Hkv <= 0 || Hq <= 0) return FORGE_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FORGE_ERR_UNSUPPORTED;
+  const int64_t G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return FORGE_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FORGE_ERR_VALUE;
+  if (T == 0 || B == 0) return FORGE_OK;
+  FORGE_TRY(check_vec16(q, 2));
+  FORGE_TRY(check_vec16(out, out->dtype == FORGE_BF16 ? 2 : 4));
+  if (!block_tables->data || !context_lens->data || !query_start->data) return FORGE_ERR_NULL;
+  if (block_tables->stride[1] != 1 || context_lens->stride[0] != 1 || query_start->stride[0] != 1)
+    return FORGE_ERR_SHAPE;
+  if (NB > 0 && (!k_cache->data || !v_cache->data)) return FORGE_ERR_NULL;
+
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  FORGE_TRY(current_device(&dev));
+  FORGE_TRY(device_state(dev, &err, &sms));
+  forge::PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q->data);
+  p.q_st = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_sb = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.query_start = static_cast<const int32_t*>(query_start->data);
+  p.out = out->data;
+  p.o_st = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.B = static_cast<int>(B);
+  p.Hq = static_cast<int>(Hq);
+  p.Hkv = static_cast<int>(Hkv);
+  p.NB = static_cast<int>(NB);
+  p.MB = static_cast<int>(MB);
+  p.T = static_cast<int>(T);
+  p.qk_scale_log2 = scale * 1.4426950408889634f;
+  p.err = err;
+  CUtensorMap tmk, tmv;
+  FORGE_TRY(encode_cache_map(k_cache, &tmk));
+  FORGE_TRY(encode_cache_map(v_cache, &tmv));
+  if (forge::launch_prefill(p, tmk, tmv, static_cast<int>(D), static_cast<int>(G), out->dtype == FORGE_BF16,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FORGE_ERR_CUDA;
+  return FORGE_OK;
+}
+
 const char* forge_status_string(int status) {
   switch (status) {
     case FORGE_OK: return "FORGE_OK";

@@ -21,6 +21,7 @@ constexpr int kDevErrLength = 2;
 constexpr int kDevErrSlot = 3;
 constexpr int kDevErrTimeout = 4;
 constexpr int kDevErrPosition = 5;
+constexpr int kDevErrQuery = 6;
 
 // A wait on a pipeline barrier gives up after this long (ns of %globaltimer).
 // A copy of a few KiB completes in microseconds; reaching this means a bug,
@@ -74,6 +75,23 @@ struct DecodeParams {
   float norm_eps;
   const float* rope;
   int rope_rows;
+  int* err;
+};
+
+// Paged prefill: the query tokens of sequence b are rows query_start[b] ..
+// query_start[b+1]-1 of q / out, at the last n_b positions of its L_b
+// cached tokens.
+struct PrefillParams {
+  const __nv_bfloat16* q;
+  int64_t q_st, q_sh;          // token, head strides (elements)
+  const int32_t* block_tables;
+  int64_t bt_sb;
+  const int32_t* context_lens;
+  const int32_t* query_start;  // [B + 1]
+  void* out;
+  int64_t o_st, o_sh;
+  int B, Hq, Hkv, NB, MB, T;
+  float qk_scale_log2;
   int* err;
 };
 
@@ -222,10 +240,41 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
-// Launchers (defined in append.cu / decode.cu).
+// Round two floats to bf16 and pack them (x0 in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
+// x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// A (block, head) K or V tile of 16 tokens x D bf16 in shared memory, as the
+// TMA engine writes it from the cache's tensor map: D/64 boxes of 16 rows x
+// 128 bytes, each with the 128-byte swizzle.
+constexpr int kBoxDims = 64;                          // dims per box: one 128-byte swizzle span
+constexpr int kBoxBytes = kBlockSize * kBoxDims * 2;  // 2 KiB
+
+// Shared-memory address of 16-byte chunk `chunk` (of D/8) in row `row` of
+// such a tile: box = chunk / 8, and within a box the chunk index is XORed
+// with the row index mod 8.
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * kBoxBytes + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
+}
+
+// Launchers (defined in append.cu / decode.cu / prefill.cu).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int D, int G,
                           bool out_bf16, cudaStream_t stream);
 size_t decode_smem_bytes(int D, int G, int bps, int nstage);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int D, int G,
+                           bool out_bf16, cudaStream_t stream);
 
 }  // namespace forge

@@ -47,8 +47,6 @@ constexpr int kStageBlocks = 2;              // KV blocks (tiles) per pipeline s
 constexpr int kConsumerWarps = kStageBlocks; // one tile per consumer warp per stage
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;    // + one producer warp
-constexpr int kBoxDims = 64;                 // dims per TMA box: 128 bytes, one swizzle span
-constexpr int kBoxBytes = kBlockSize * kBoxDims * 2;  // 2 KiB: 16 rows of 128 B
 
 struct SmemLayout {
   size_t ring, logits, red_ml, bars, total;
@@ -92,13 +90,6 @@ __device__ __forceinline__ int checked_length(const DecodeParams& p, int b, bool
   return L;
 }
 
-// Shared-memory address of 16-byte chunk `chunk` (of D/8) in row `row` of a
-// tile stored as D/64 swizzled boxes: box = chunk / 8, and within a box the
-// chunk index is XORed with the row index mod 8 (TMA 128-byte swizzle).
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
-  return tile + (chunk >> 3) * kBoxBytes + row * 128 + ((((chunk & 7) ^ (row & 7))) << 4);
-}
-
 // Fused append: put this step's new row (`src`, D bf16) into row `r` of the
 // staged swizzled tile at `tile`, and into the cache row `cache_row` (when
 // not null), 16 bytes per lane.  Then order the shared-memory writes before
@@ -113,11 +104,6 @@ __device__ __forceinline__ void patch_new_row(unsigned char* tile, const __nv_bf
   }
   fence_proxy_async_smem();
   __syncwarp();
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // The q/k path ("Make the Engine Talk", 1.3: RMSNorm and rotary position
@@ -218,16 +204,6 @@ __device__ __forceinline__ void patch_new_k_row(unsigned char* tile, const __nv_
   }
   fence_proxy_async_smem();
   __syncwarp();
-}
-
-// Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
-// x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // Split reduce for the G heads of (b, g): with M = max_s m_s and

@@ -203,3 +203,39 @@ def test_qk_options_are_validated(lib):
     if expect is not None:   # valid options reach CUDA (absent here)
         assert call(q_norm_weight=_desc([64], BF16), k_norm_weight=_desc([64], BF16),
                     rope_cos_sin=_desc([10, 64], F32)) == -6
+
+
+def _prefill_args(**over):
+    a = dict(q=_desc([10, 8, 64], BF16), k=_desc([8, 2, 16, 64], BF16), v=_desc([8, 2, 16, 64], BF16),
+             bt=_desc([2, 4], I32), cl=_desc([2], I32), qs=_desc([3], I32), scale=0.125,
+             out=_desc([10, 8, 64], F32))
+    a.update(over)
+    return a
+
+
+def _call_prefill(lib, a):
+    r = lambda d: ctypes.byref(d) if d is not None else None
+    return lib.forge_paged_prefill(r(a["q"]), r(a["k"]), r(a["v"]), r(a["bt"]), r(a["cl"]), r(a["qs"]),
+                                   a["scale"], r(a["out"]), None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qs=None), -1),
+    (dict(qs=_desc([3], I64)), -2),
+    (dict(qs=_desc([2], I32)), -3),                                                 # not B + 1 entries
+    (dict(out=_desc([9, 8, 64], F32)), -3),                                         # not T rows
+    (dict(bt=_desc([3, 4], I32)), -3),
+    (dict(q=_desc([10, 8, 96], BF16), k=_desc([8, 2, 16, 96], BF16), v=_desc([8, 2, 16, 96], BF16),
+          out=_desc([10, 8, 96], F32)), -4),                                        # D = 96
+    (dict(q=_desc([10, 32, 64], BF16), out=_desc([10, 32, 64], F32)), -4),         # G = 16
+    (dict(scale=float("inf")), -8),
+    (dict(q=_desc([10, 8, 64], BF16, data=8)), -5),
+    (dict(qs=_desc([3], I32, stride=[2])), -3),
+])
+def test_prefill_rejects_bad_arguments(lib, over, status):
+    assert _call_prefill(lib, _prefill_args(**over)) == status
+
+
+def test_prefill_empty_is_a_no_op(lib):
+    a = _prefill_args(q=_desc([0, 8, 64], BF16, data=0), out=_desc([0, 8, 64], F32, data=0))
+    assert _call_prefill(lib, a) == 0

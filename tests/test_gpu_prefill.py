@@ -1,0 +1,164 @@
+"""forge_paged_prefill on the GPU against the oracle's prefill.
+
+Each case appends the run's K/V with forge_paged_kv_append (one slot per
+token; bit-exact against the oracle's append), then runs the prefill and
+compares every output row with oracle.paged_prefill within the parity
+tolerance.  Covers every instantiation (D 64 / 128, G 1 / 2 / 4 / 8, fp32 /
+bf16 out), runs that are whole prompts, single tokens, empty, or cross block
+and stage boundaries, the Qwen3-4B-shaped batch at full size (sampled
+sequences), graph capture, and the device-side check of query_start.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import DEV, TOL, bf16_dev, bits_host, max_abs_err
+from paged_kv_gqa_06_gb300 import binding
+from paged_kv_gqa_06_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.init()
+
+
+class DevicePrefill:
+    def __init__(self, pw, t):
+        self.pw = pw
+        self.q = bf16_dev(t["q"])
+        self.k_new = bf16_dev(t["k_new"])
+        self.v_new = bf16_dev(t["v_new"])
+        self.k_cache = bf16_dev(t["k_cache"])
+        self.v_cache = bf16_dev(t["v_cache"])
+        self.slots = torch.from_numpy(pw.slot_mapping).to(DEV)
+        self.tables = torch.from_numpy(pw.block_tables).to(DEV)
+        self.lens = torch.from_numpy(pw.context_lens).to(DEV)
+        self.qs = torch.from_numpy(pw.query_start).to(DEV)
+
+    def append(self):
+        binding.forge_paged_kv_append(self.k_new, self.v_new, self.slots, self.k_cache, self.v_cache)
+
+    def prefill(self, out_dtype, stream=None):
+        dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+        out = torch.full((self.pw.T, self.pw.Hq, self.pw.D), float("nan"), dtype=dt, device=DEV)
+        binding.forge_paged_prefill(self.q, self.k_cache, self.v_cache, self.tables, self.lens, self.qs,
+                                    self.pw.scale, out, stream=stream)
+        return out
+
+
+def _oracle(pw, t):
+    kc, vc = t["k_cache"].copy(), t["v_cache"].copy()
+    oracle.paged_kv_append(t["k_new"], t["v_new"], pw.slot_mapping, kc, vc)
+    return kc, vc, oracle.paged_prefill(t["q"], kc, vc, pw.block_tables, pw.context_lens, pw.query_start, pw.scale)
+
+
+def _check(pw, out_dtypes=("f32", "bf16")):
+    t = pw.layer(0)
+    kc, vc, ref = _oracle(pw, t)
+    d = DevicePrefill(pw, t)
+    d.append()
+    assert np.array_equal(bits_host(d.k_cache), kc) and np.array_equal(bits_host(d.v_cache), vc)
+    for od in out_dtypes:
+        out = d.prefill(od)
+        err = max_abs_err(out, ref)
+        assert err <= TOL[od], f"{od}: max abs err {err}"
+    assert binding.forge_paged_get_device_error() == 0
+
+
+def test_prefill_tiny():
+    _check(W.make_prefill("prefill_tiny"))
+
+
+# lengths and runs: whole prompts, one token, empty, block (16) and stage (32) edges
+LENS = (1, 15, 16, 17, 31, 32, 33, 64, 100, 257)
+RUNS = (1, 15, 1, 17, 31, 5, 32, 64, 0, 200)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 32, 8), (128, 8, 8), (128, 16, 8), (128, 64, 8),
+                                      (64, 8, 2), (64, 16, 16), (64, 16, 8), (64, 32, 4)])
+def test_prefill_shapes(D, Hq, Hkv):
+    spec = W.custom_spec(f"pf{D}_{Hq}_{Hkv}", B=len(LENS), Hq=Hq, Hkv=Hkv, D=D, fixed_lens=LENS, free_frac=0.2,
+                         seed=400 + Hq + D)
+    _check(W.make_prefill(spec, chunk_lens=RUNS))
+
+
+def test_whole_prompts_and_long_runs():
+    spec = W.custom_spec("pf_whole", B=3, Hq=32, Hkv=8, D=128, fixed_lens=(700, 129, 1000), free_frac=0.1,
+                         seed=411, k_mul=2.0)
+    _check(W.make_prefill(spec))                            # every token a query
+    _check(W.make_prefill(spec, chunk_lens=(300, 129, 77)))
+
+
+def test_one_token_runs_match_the_decode():
+    spec = W.custom_spec("pf_dec", B=6, Hq=32, Hkv=8, D=128, fixed_lens=(1, 16, 17, 500, 2049, 33), seed=412)
+    pw = W.make_prefill(spec, chunk_lens=(1,) * 6)
+    t = pw.layer(0)
+    d = DevicePrefill(pw, t)
+    d.append()
+    pre = d.prefill("f32")
+    dec = torch.empty_like(pre)
+    binding.forge_paged_gqa_decode(d.q, d.k_cache, d.v_cache, d.tables, d.lens, pw.scale, dec)
+    _, _, ref = _oracle(pw, t)
+    assert max_abs_err(pre, ref) <= TOL["f32"] and max_abs_err(dec, ref) <= TOL["f32"]
+
+
+def test_prefill_qwen3_4b_full_size_sampled():
+    pw = W.make_prefill("prefill_4b")
+    t = pw.layer(0)
+    d = DevicePrefill(pw, t)
+    d.append()
+    out = d.prefill("bf16")
+    torch.cuda.synchronize()
+    assert binding.forge_paged_get_device_error() == 0
+    kc, vc = bits_host(d.k_cache), bits_host(d.v_cache)
+    kc_ref, vc_ref = t["k_cache"].copy(), t["v_cache"].copy()
+    oracle.paged_kv_append(t["k_new"], t["v_new"], pw.slot_mapping, kc_ref, vc_ref)
+    assert np.array_equal(kc, kc_ref) and np.array_equal(vc, vc_ref)
+    for b in (0, 3, 7):                                    # sampled sequences, all their query rows
+        q0, q1 = int(pw.query_start[b]), int(pw.query_start[b + 1])
+        ref = oracle.paged_prefill(t["q"][q0:q1], kc_ref, vc_ref, pw.block_tables[b:b + 1],
+                                   pw.context_lens[b:b + 1], np.array([0, q1 - q0], np.int32), pw.scale)
+        assert max_abs_err(out[q0:q1], ref) <= TOL["bf16"], b
+
+
+def test_prefill_graph_capture():
+    pw = W.make_prefill("prefill_tiny")
+    t = pw.layer(0)
+    _, _, ref = _oracle(pw, t)
+    d = DevicePrefill(pw, t)
+    d.append()
+    out = torch.full((pw.T, pw.Hq, pw.D), float("nan"), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.forge_paged_prefill(d.q, d.k_cache, d.v_cache, d.tables, d.lens, d.qs, pw.scale, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert max_abs_err(out, ref) <= TOL["f32"]
+
+
+def test_bad_query_start_is_flagged_and_rows_untouched():
+    pw = W.make_prefill("prefill_tiny")
+    t = pw.layer(0)
+    d = DevicePrefill(pw, t)
+    d.append()
+    assert binding.forge_paged_get_device_error() == 0
+    qs = pw.query_start.copy()
+    qs[1:] = np.minimum(qs[1:] + 5, pw.T)                # sequence 0 now claims 25 rows of a 20-token context
+    d.qs = torch.from_numpy(qs).to(DEV)
+    out = d.prefill("f32")
+    assert binding.forge_paged_get_device_error() == 6
+    assert torch.isnan(out[: qs[1]]).all()                 # sequence 0's rows were not written
+
+
+def test_empty_batch_is_a_no_op():
+    pw = W.make_prefill("prefill_tiny", chunk_lens=(0, 0, 0, 0))
+    d = DevicePrefill(pw, pw.layer(0))
+    out = torch.empty(0, pw.Hq, pw.D, dtype=torch.float32, device=DEV)
+    binding.forge_paged_prefill(d.q, d.k_cache, d.v_cache, d.tables, d.lens, d.qs, pw.scale, out)
+    assert binding.forge_paged_get_device_error() == 0

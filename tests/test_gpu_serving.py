@@ -6,7 +6,8 @@ bit for bit; and a whole serving loop -- requests arriving, prompts written
 into their blocks on admission, one appended token and one decode per
 running row per step, retirement and preemption -- must give decode outputs
 within the parity tolerance of the CPU oracle run over the oracle's own
-tables, with the caches bit-identical at the end.
+tables, with the caches bit-identical at the end.  Admitted prompts go
+through forge_paged_prefill, checked against the oracle's prefill.
 """
 import numpy as np
 import pytest
@@ -151,23 +152,37 @@ def test_serving_loop_matches_the_oracle(mode):
         with torch.cuda.graph(graph, stream=side):
             launch()
 
-    retired, step, errs = 0, 0, []
+    retired, step, errs, prefilled = 0, 0, [], 0
     while retired < len(stream.seq_ids):
         for req in stream.arriving(step):
             d.submit(req)
         with torch.cuda.stream(side):
             want = d.step(stream=side)
         host_tables = d.host_tables()
-        # prefill stand-in: the prompt's K/V written into the blocks the driver gave it
-        for s, r, p in want["admitted"]:
-            if p == 0:
-                continue
+        # prefill of the admitted prompts: their K/V written into the blocks the
+        # driver gave them, then one forge_paged_prefill over all of them
+        pf = [(r, p) for _, r, p in want["admitted"] if p > 0]
+        for r, p in pf:
             table = d.ref.table(r)
             slots = np.array([table[t // bs] * bs + t % bs for t in range(p)], dtype=np.int64)
             k, v = _bf16(rng, (p, Hkv, D)), _bf16(rng, (p, Hkv, D))
             oracle.paged_kv_append(k, v, slots, kc_h, vc_h)
             with torch.cuda.stream(side):
                 B.forge_paged_kv_append(_dev(k), _dev(v), torch.from_numpy(slots).to(DEV), kc_d, vc_d, stream=side)
+        if pf:
+            pf_tables = np.ascontiguousarray(host_tables[[r for r, _ in pf]])
+            pf_lens = np.array([p for _, p in pf], dtype=np.int32)
+            pf_qs = np.concatenate([[0], np.cumsum(pf_lens)]).astype(np.int32)
+            pq = _bf16(rng, (int(pf_qs[-1]), Hq, D))
+            pf_ref = oracle.paged_prefill(pq, kc_h, vc_h, pf_tables, pf_lens, pf_qs, scale)
+            pf_out = torch.empty(int(pf_qs[-1]), Hq, D, dtype=torch.float32, device=DEV)
+            with torch.cuda.stream(side):
+                B.forge_paged_prefill(_dev(pq), kc_d, vc_d, torch.from_numpy(pf_tables).to(DEV),
+                                      torch.from_numpy(pf_lens).to(DEV), torch.from_numpy(pf_qs).to(DEV), scale,
+                                      pf_out, stream=side)
+            side.synchronize()
+            prefilled += len(pf)
+            errs.append(float(np.max(np.abs(pf_out.double().cpu().numpy() - pf_ref))))
         # this step's token of every running row, then the decode
         q, kn, vn = _bf16(rng, (rows, Hq, D)), _bf16(rng, (rows, Hkv, D)), _bf16(rng, (rows, Hkv, D))
         oracle.paged_kv_append(kn, vn, np.array(want["slots"], dtype=np.int64), kc_h, vc_h)
@@ -191,6 +206,7 @@ def test_serving_loop_matches_the_oracle(mode):
         retired += len(want["retired"])
         step += 1
 
+    assert prefilled > 0
     assert max(errs) <= TOL["f32"], max(errs)
     assert np.array_equal(bits_host(kc_d), kc_h) and np.array_equal(bits_host(vc_d), vc_h)
     assert B.forge_paged_get_device_error() == 0
