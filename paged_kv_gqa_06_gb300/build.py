@@ -17,8 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libforge_paged.so")
-SOURCES = ["abi.cu", "append.cu", "decode.cu", "noalloc.cu", "prefill.cu", "serving.cu"]
-HEADERS = ["common.cuh"]
+SOURCES = ["abi.cu", "append.cu", "decode.cu", "noalloc.cu", "prefill.cu", "prefill_tc.cu", "serving.cu"]
+HEADERS = ["common.cuh", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

@@ -147,6 +147,31 @@ int encode_cache_map(const forge_tensor* c, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_UNSUPPORTED;
 }
 
+// Tensor map over the prefill's q [T, Hq, D] bf16, dims innermost first
+// (D, head, token), boxes of 64 dims x G heads x 128/G tokens: one box is the
+// 128 K-major rows (token-major, head-minor) of the tcgen05 kernel's Q tile,
+// with the 128-byte swizzle.  Rows past T read as zeros.
+int encode_q_map(const forge_tensor* q, int G, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return FORGE_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(q->shape[2]), static_cast<cuuint64_t>(q->shape[1]),
+                              static_cast<cuuint64_t>(q->shape[0])};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(q->stride[1]) * 2, static_cast<cuuint64_t>(q->stride[0]) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_UNSUPPORTED;
+}
+
+// Which prefill kernel: the tcgen05 one unless FORGE_PREFILL_KERNEL=mma
+// selects the mma.sync one (kept for comparison).
+bool prefill_use_mma_sync() {
+  const char* e = std::getenv("FORGE_PREFILL_KERNEL");
+  return e && std::strcmp(e, "mma") == 0;
+}
+
 int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms) {
   if (split_tokens > 0) return split_tokens / kBlockSize;
   // Automatic: 512-token splits, shortened while the upper bound on CTAs
@@ -597,10 +622,17 @@ int forge_paged_prefill(const forge_tensor* q, const forge_tensor* k_cache, cons
   CUtensorMap tmk, tmv;
   FORGE_TRY(encode_cache_map(k_cache, &tmk));
   FORGE_TRY(encode_cache_map(v_cache, &tmv));
-  if (forge::launch_prefill(p, tmk, tmv, static_cast<int>(D), static_cast<int>(G), out->dtype == FORGE_BF16,
-                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FORGE_ERR_CUDA;
-  return FORGE_OK;
+  cudaError_t e;
+  if (prefill_use_mma_sync()) {
+    e = forge::launch_prefill(p, tmk, tmv, static_cast<int>(D), static_cast<int>(G), out->dtype == FORGE_BF16,
+                              static_cast<cudaStream_t>(stream));
+  } else {
+    CUtensorMap tmq;
+    FORGE_TRY(encode_q_map(q, static_cast<int>(G), &tmq));
+    e = forge::launch_prefill_tc(p, tmq, tmk, tmv, static_cast<int>(D), static_cast<int>(G),
+                                 out->dtype == FORGE_BF16, static_cast<cudaStream_t>(stream));
+  }
+  return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA;
 }
 
 const char* forge_status_string(int status) {

@@ -143,8 +143,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the barrier phase with this parity has completed.  Returns false
 // (after recording kDevErrTimeout) if that takes longer than kWaitLimitNs.
+// Once a wait has timed out anywhere, later waits give up at once, so a
+// broken pipeline ends quickly instead of spending the limit at every wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (err && *reinterpret_cast<volatile int*>(err) == kDevErrTimeout) return false;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -163,6 +166,15 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// One tiled box of a 3-D tensor map into shared memory (as tma_load_4d).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -276,5 +288,9 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, cons
 size_t decode_smem_bytes(int D, int G, int bps, int nstage);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int D, int G,
                            bool out_bf16, cudaStream_t stream);
+// The same prefill on the 5th-generation tensor cores; tmap_q is a 3-D map
+// over q [T, Hq, D] with boxes of 64 dims x G heads x (128 / G) tokens.
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, int D, int G, bool out_bf16, cudaStream_t stream);
 
 }  // namespace forge

@@ -1,4 +1,5 @@
-"""forge_paged_prefill on the GPU against the oracle's prefill.
+"""forge_paged_prefill on the GPU against the oracle's prefill, for both
+kernels behind it (tcgen05 and mma.sync).
 
 Each case appends the run's K/V with forge_paged_kv_append (one slot per
 token; bit-exact against the oracle's append), then runs the prefill and
@@ -25,6 +26,16 @@ def _built():
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.init()
+
+
+@pytest.fixture(params=["tcgen05", "mma_sync"], autouse=True)
+def kernel(request, monkeypatch):
+    """Both prefill kernels: the tcgen05 one (default) and the mma.sync one."""
+    if request.param == "mma_sync":
+        monkeypatch.setenv("FORGE_PREFILL_KERNEL", "mma")
+    else:
+        monkeypatch.delenv("FORGE_PREFILL_KERNEL", raising=False)
+    return request.param
 
 
 class DevicePrefill:
