@@ -16,22 +16,29 @@
 //   * warp 5 (MMA) owns 256 TMEM columns: S in two 64-column buffers and the
 //     output accumulator O (D columns).  Its lane 0 issues S_j = Q K_j^T
 //     (M 128, N 64, K = D; Q and K K-major straight from the TMA layout) and
-//     then O += P_{j-1} V_{j-1} for the previous tile (M 128, N = D, K 64;
-//     P K-major from shared memory, V MN-major as it lies in the stage), so
-//     that S of the next tile is computed while the softmax works on this
-//     one; tcgen05.commit on mbarriers tracks completion and frees stages;
+//     O += P_j V_j (M 128, N = D, K 64; P read from TMEM, where the softmax
+//     wrote it over its S buffer; V MN-major as it lies in the stage), each
+//     as soon as its inputs are ready, so the tensor cores compute S of the
+//     next tile while the softmax works on this one; tcgen05.commit on
+//     mbarriers tracks completion and frees stages and buffers;
 //   * warps 0-3 (softmax) own one row each (warp w reads TMEM lanes
-//     32w..32w+31).  Per tile: load the row of S, apply the causal mask by
-//     position and the scale in log2 units, and keep a running maximum that
-//     only moves when the row's maximum grows by more than 8 (2^8 headroom
-//     in the weights), so O in TMEM is rescaled rarely; write
-//     P = 2^(s - m) to shared memory as bf16 high and low parts (two MMAs keep
-//     ~16 bits of each weight, as in the decode); at the end divide O by the
-//     row sum and store the row.
+//     32w..32w+31).  Per tile: load the row of S, mask by position (only on
+//     tiles that reach past the row's position), and keep a running maximum
+//     that only moves when the row's maximum grows by more than 8 in log2
+//     units, so the weights stay <= 2^8 and O in TMEM is rescaled rarely.
+//     The weights P = 2^(scale s - m) are split into bf16 high and low parts
+//     (two MMAs keep ~16 bits of each weight, as in the decode) and stored
+//     over the row's S in TMEM (high in the buffer's first 32 columns, low in
+//     the next 32, two weights per column); the softmax waits on the tensor
+//     cores only when O has to be rescaled.  At the end O is divided by the
+//     row sum and stored.
+// Shared memory is 98 KB and TMEM 256 columns per CTA, so two CTAs share an
+// SM: while one CTA's softmax runs, the other's MMAs keep the tensor cores
+// busy.
 // V rows that may hold anything (the tail of the last block, or blocks the
 // last stage did not load) are zeroed before P V reads them: P is 0 there,
 // but 0 * NaN is NaN.  Every mbarrier wait is bounded; the MMA warp drains
-// its own MMAs before freeing TMEM.
+// its own MMAs before TMEM is freed.
 #include <atomic>
 
 #include "common.cuh"
@@ -42,7 +49,7 @@ namespace {
 
 constexpr int kTcRows = 128;                 // MMA M
 constexpr int kTcKv = 64;                    // tokens per stage (MMA N of S, K of P V)
-constexpr int kTcStages = 2;
+constexpr int kTcStages = 2;                 // K/V ring depth
 constexpr int kTcThreads = 6 * 32;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 256;
@@ -51,25 +58,30 @@ constexpr float kRescaleSlack = 8.0f;        // log2 units: weights stay <= 2^8
 constexpr unsigned kFullMask = 0xffffffffu;
 
 struct TcLayout {
-  int q, kv, p_hi, p_lo, bars, total;
+  int q, kv, bars, total;
 };
 
-// Q [BOXES][128 rows][128 B] | stages [K: BOXES][64][128 B], [V: same] |
-// P_hi [128][128 B] | P_lo | mbarriers, TMEM slot.  Offsets from a
-// 1024-byte-aligned base.
+// Q [BOXES][128 rows][128 B] | kTcStages x ([K: BOXES][64][128 B], [V: same]) |
+// mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.
 __host__ __device__ constexpr TcLayout tc_layout(int D) {
   const int boxes = D / 64;
   TcLayout l{};
   l.q = 0;
   l.kv = l.q + boxes * kTcRows * 128;
-  l.p_hi = l.kv + kTcStages * 2 * boxes * kTcKv * 128;
-  l.p_lo = l.p_hi + kTcRows * 128;
-  l.bars = l.p_lo + kTcRows * 128;
+  l.bars = l.kv + kTcStages * 2 * boxes * kTcKv * 128;
   l.total = l.bars + 16 * 8 + 1024;          // barriers + slot, + alignment slack
   return l;
 }
 
-enum Bar { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kPvDone = 10, kDrain = 11 };
+// mbarrier slots
+constexpr int kQFull = 0;
+constexpr int kKvFull = 1;                   // [kTcStages]
+constexpr int kKvEmpty = kKvFull + kTcStages;
+constexpr int kSFull = kKvEmpty + kTcStages; // [2]: S_j written
+constexpr int kPFull = kSFull + 2;           // [2]: P_j written over S_j
+constexpr int kPvDone = kPFull + 2;          // [2]: P_j V_j done, S/P buffer free
+constexpr int kDrain = kPvDone + 2;
+constexpr int kSlot = kDrain + 1;            // TMEM address (4 bytes) after the barriers
 
 // 32 consecutive outputs of a row: fp32 accumulators times `inv`.
 __device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], float inv) {
@@ -89,12 +101,40 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   }
 }
 
-__device__ __forceinline__ float sel_scale(float s, int t, int lim, float scale) {
-  return t <= lim ? s * scale : -INFINITY;
+// Find (sequence, first query token) of tile `tile_id` from query_start: a
+// warp scan over the sequences' tile counts, the same answer in every warp.
+template <int QT>
+__device__ __forceinline__ void find_tile(const PrefillParams& p, int tile_id, int lane, int& b, int& i0) {
+  b = -1;
+  i0 = 0;
+  int base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int bb = b0 + lane;
+    int nt = 0;
+    if (bb < p.B) {
+      const int n = __ldg(p.query_start + bb + 1) - __ldg(p.query_start + bb);
+      nt = n > 0 ? (n + QT - 1) / QT : 0;
+    }
+    int incl = nt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int total = __shfl_sync(kFullMask, incl, 31);
+    if (tile_id < base + total) {
+      const int first = __ffs(__ballot_sync(kFullMask, tile_id < base + incl)) - 1;
+      const int before = __shfl_sync(kFullMask, incl - nt, first);
+      b = b0 + first;
+      i0 = (tile_id - base - before) * QT;
+      return;
+    }
+    base += total;
+  }
 }
 
 template <int D, int G, typename OutT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   constexpr int QT = kTcRows / G;            // query tokens per CTA
@@ -106,7 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kTcRows, D, true);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
-  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later (longer) tiles first
 
   // query_start must start at 0, never decrease and end within the T rows
   if (blockIdx.x == 0 && g == 0 && warp == 0) {
@@ -118,34 +158,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (__any_sync(kFullMask, bad) && lane == 0) record_error(p.err, kDevErrQuery);
   }
 
-  // ---- the sequence and first query token of this tile (every warp finds the same)
-  int b = -1, i0 = 0;
-  {
-    int base = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-      const int bb = b0 + lane;
-      int nt = 0;
-      if (bb < p.B) {
-        const int n = __ldg(p.query_start + bb + 1) - __ldg(p.query_start + bb);
-        nt = n > 0 ? (n + QT - 1) / QT : 0;
-      }
-      int incl = nt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off) incl += v;
-      }
-      const int total = __shfl_sync(kFullMask, incl, 31);
-      if (tile_id < base + total) {
-        const int first = __ffs(__ballot_sync(kFullMask, tile_id < base + incl)) - 1;
-        const int before = __shfl_sync(kFullMask, incl - nt, first);
-        b = b0 + first;
-        i0 = (tile_id - base - before) * QT;
-        break;
-      }
-      base += total;
-    }
-  }
+  int b, i0;
+  find_tile<QT>(p, tile_id, lane, b, i0);
   if (b < 0) return;  // past the last tile
 
   const int q0 = __ldg(p.query_start + b);
@@ -164,18 +178,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                        ~static_cast<uintptr_t>(1023));
   const uint32_t sm_s = smem_addr(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + lay.bars + 12 * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kSlot);
 
   if (threadIdx.x == 0) {
     mbar_init(bars + kQFull, 1);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(bars + kKvFull + i, 1);
       mbar_init(bars + kKvEmpty + i, 1);
-      mbar_init(bars + kSFull + i, 1);
-      mbar_init(bars + kSFree + i, 4);   // one arrival per softmax warp
     }
-    mbar_init(bars + kPFull, 4);
-    mbar_init(bars + kPvDone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + kSFull + i, 1);
+      mbar_init(bars + kPFull + i, 4);   // one arrival per softmax warp
+      mbar_init(bars + kPvDone + i, 1);
+    }
     mbar_init(bars + kDrain, 1);
     fence_barrier_init();
   }
@@ -197,8 +212,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_3d(sm + lay.q + c * kTcRows * 128, &tmq, c * 64, g * G, q0 + i0, bars + kQFull);
       const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
       for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        if (j >= kTcStages) mbar_wait(bars + kKvEmpty + st, ((j >> 1) & 1) ^ 1u, p.err);
+        const int st = j % kTcStages, use = j / kTcStages;
+        if (use > 0) mbar_wait(bars + kKvEmpty + st, (use - 1) & 1, p.err);  // stage released by P V
         unsigned char* kst = sm + lay.kv + st * 2 * KV_HALF;
         int pb[4];
         uint32_t bytes = 0;
@@ -235,39 +250,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issue
+    // Issue each MMA group as soon as its inputs are ready, whichever comes
+    // first: S_j = Q K_j^T needs stage j loaded and S buffer j % 2 free
+    // (P_{j-2} V done); O += P_j V_j needs P_j written.  Waiting for one
+    // would hold back the other and stall the ring.
     if (lane == 0) {
       mbar_wait(bars + kQFull, 0, p.err);
       tc::fence_after_sync();
-      for (int j = 0; j <= nkv; ++j) {
-        if (j < nkv) {
-          const int st = j & 1;
-          mbar_wait(bars + kKvFull + st, (j >> 1) & 1, p.err);
-          if (j >= kTcStages) mbar_wait(bars + kSFree + st, ((j >> 1) & 1) ^ 1u, p.err);
-          tc::fence_after_sync();
-          const uint32_t kst = sm_s + lay.kv + st * 2 * KV_HALF;
+      int next_qk = 0, next_pv = 0;
+      uint64_t last = global_timer_ns();
+      while (next_pv < nkv) {
+        bool progressed = false;
+        if (next_qk < nkv && next_qk <= next_pv + 1) {
+          const int j = next_qk, st = j % kTcStages, sb = j & 1;
+          if (mbar_try_wait(bars + kKvFull + st, (j / kTcStages) & 1) &&
+              (j < 2 || mbar_try_wait(bars + kPvDone + sb, ((j >> 1) - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint32_t kst = sm_s + lay.kv + st * 2 * KV_HALF;
 #pragma unroll
-          for (int k = 0; k < KSTEPS; ++k) {
-            const uint64_t a = tc::smem_desc_sw128(sm_s + lay.q + (k >> 2) * kTcRows * 128 + (k & 3) * 32, 0, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
-            tc::mma_bf16_ss(tmem + st * kTcKv, a, bd, IDESC_S, k > 0);
+            for (int k = 0; k < KSTEPS; ++k) {
+              const uint64_t a = tc::smem_desc_sw128(sm_s + lay.q + (k >> 2) * kTcRows * 128 + (k & 3) * 32, 0, 1024);
+              const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
+              tc::mma_bf16_ss(tmem + sb * kTcKv, a, bd, IDESC_S, k > 0);
+            }
+            tc::commit(smem_addr(bars + kSFull + sb));
+            ++next_qk;
+            progressed = true;
           }
-          tc::commit(smem_addr(bars + kSFull + st));
         }
-        if (j >= 1) {
-          const int jp = j - 1, stp = jp & 1;
-          mbar_wait(bars + kPFull, jp & 1, p.err);
-          tc::fence_after_sync();
-          const uint32_t vst = sm_s + lay.kv + stp * 2 * KV_HALF + KV_HALF;
+        if (next_pv < next_qk) {
+          const int jp = next_pv, pbuf = jp & 1, stp = jp % kTcStages;
+          if (mbar_try_wait(bars + kPFull + pbuf, (jp >> 1) & 1)) {
+            tc::fence_after_sync();
+            const uint32_t vst = sm_s + lay.kv + stp * 2 * KV_HALF + KV_HALF;
+            const uint32_t phi = tmem + pbuf * kTcKv, plo = phi + kTcKv / 2;  // P over S in TMEM
 #pragma unroll
-          for (int kk = 0; kk < kTcKv / 16; ++kk) {
-            const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
-            tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sm_s + lay.p_hi + kk * 32, 0, 1024), bd, IDESC_O,
-                            jp > 0 || kk > 0);
-            tc::mma_bf16_ss(tmem + kColO, tc::smem_desc_sw128(sm_s + lay.p_lo + kk * 32, 0, 1024), bd, IDESC_O,
-                            true);
+            for (int kk = 0; kk < kTcKv / 16; ++kk) {
+              const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
+              tc::mma_bf16_ts(tmem + kColO, phi + 8 * kk, bd, IDESC_O, jp > 0 || kk > 0);
+              tc::mma_bf16_ts(tmem + kColO, plo + 8 * kk, bd, IDESC_O, true);
+            }
+            tc::commit(smem_addr(bars + kPvDone + pbuf));
+            tc::commit(smem_addr(bars + kKvEmpty + stp));
+            ++next_pv;
+            progressed = true;
           }
-          tc::commit(smem_addr(bars + kPvDone));
-          tc::commit(smem_addr(bars + kKvEmpty + stp));
+        }
+        if (progressed) {
+          last = global_timer_ns();
+        } else if (global_timer_ns() - last > kWaitLimitNs) {
+          record_error(p.err, kDevErrTimeout);
+          break;
         }
       }
       // every MMA of this thread done before TMEM is freed, whatever happened above
@@ -281,78 +314,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool ok = i0 + tok < n;
     const int lim = ok ? pos0 + tok : p_max;       // causal limit of the row
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    unsigned char* phi = sm + lay.p_hi + r * 128;
-    unsigned char* plo = sm + lay.p_lo + r * 128;
+    const float scale = p.qk_scale_log2;
     float m_used = -INFINITY, l = 0.f;             // max the weights are taken against; row sum
     for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      mbar_wait(bars + kSFull + st, (j >> 1) & 1, p.err);
+      const int sb = j & 1;
+      mbar_wait(bars + kSFull + sb, (j >> 1) & 1, p.err);
       tc::fence_after_sync();
       float s[kTcKv];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[32];
-        tc::ld_32x32b_x32(trow + st * kTcKv + 32 * h, v);
+        tc::ld_32x32b_x32(trow + sb * kTcKv + 32 * h, v);
         tc::wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[32 * h + c] = __uint_as_float(v[c]);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kSFree + st);   // S buffer may be overwritten
 
       const int t0 = j * kTcKv;
+      if (t0 + kTcKv - 1 > lim) {  // the tile reaches past this row's position
+#pragma unroll
+        for (int c = 0; c < kTcKv; ++c) s[c] = t0 + c <= lim ? s[c] : -INFINITY;
+      }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTcKv; ++c) {
-        s[c] = sel_scale(s[c], t0 + c, lim, p.qk_scale_log2);
-        mx = fmaxf(mx, s[c]);
-      }
+      for (int c = 0; c < kTcKv; ++c) mx = fmaxf(mx, s[c]);
       // every row sees token 0 in the first stage, so m_new is finite
-      const float m_new = fmaxf(m_used, mx);
+      const float m_new = fmaxf(m_used, mx * scale);
       const bool need = m_new > m_used + kRescaleSlack;
-      if (j >= 1) {
-        mbar_wait(bars + kPvDone, (j - 1) & 1, p.err);  // O is stable and the P buffers are free
-        tc::fence_after_sync();
-        if (__any_sync(kFullMask, need)) {
-          const float f = need ? fast_exp2(m_used - m_new) : 1.f;
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t v[32];
-            tc::ld_32x32b_x32(trow + kColO + 32 * c4, v);
-            tc::wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
-            tc::st_32x32b_x32(trow + kColO + 32 * c4, v);
-          }
-          tc::wait_st();
-        }
-      }
+      const float alpha = fast_exp2(m_used - m_new);  // 0 on the first stage (m_used = -inf)
       if (need) {
-        l *= fast_exp2(m_used - m_new);  // 0 on the first stage (m_used = -inf)
+        l *= alpha;
         m_used = m_new;
       }
-      // P = 2^(s - m_used) <= 2^8, as bf16 high and low parts; 16-byte chunk q
-      // of the row holds tokens 8q .. 8q+7 (128-byte swizzle)
+      if (j >= 1 && __any_sync(kFullMask, need)) {
+        // rescale O: every P V so far (the last is tile j-1) must be finished
+        mbar_wait(bars + kPvDone + ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err);
+        tc::fence_after_sync();
+        const float f = need ? alpha : 1.f;
 #pragma unroll
-      for (int q = 0; q < kTcKv / 8; ++q) {
-        uint32_t hi[4], lo[4];
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(trow + kColO + 32 * c4, v);
+          tc::wait_ld();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = fast_exp2(s[8 * q + 2 * e] - m_used), c = fast_exp2(s[8 * q + 2 * e + 1] - m_used);
+          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
+          tc::st_32x32b_x32(trow + kColO + 32 * c4, v);
+        }
+        tc::wait_st();
+      }
+      // P = 2^(scale s - m_used) <= 2^8 as bf16 high and low parts, over S in
+      // TMEM: high in columns [0, 32) of the buffer, low in [32, 64), two
+      // weights per column; in two halves of 32 weights
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float a = fast_exp2(fmaf(s[32 * h + 2 * e], scale, -m_used));
+          const float c = fast_exp2(fmaf(s[32 * h + 2 * e + 1], scale, -m_used));
           l += a + c;
           split_bf16x2(a, c, hi[e], lo[e]);
         }
-        const int off = (q ^ (r & 7)) << 4;
-        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        tc::st_32x32b_x16(trow + sb * kTcKv + 16 * h, hi);
+        tc::st_32x32b_x16(trow + sb * kTcKv + kTcKv / 2 + 16 * h, lo);
       }
+      tc::wait_st();
       if (j == nkv - 1) {
         // V rows from z0 on may hold anything: past the sequence, or not loaded
         const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
         const int z0 = min(L - t0, loaded);
         if (z0 < kTcKv) {
-          unsigned char* vst = sm + lay.kv + st * 2 * KV_HALF + KV_HALF;
+          unsigned char* vst = sm + lay.kv + (j % kTcStages) * 2 * KV_HALF + KV_HALF;
           for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kSoftmaxThreads) {
             const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
             *reinterpret_cast<uint4*>(vst + (rest >> 3) * kTcKv * 128 + vr * 128 + (rest & 7) * 16) =
@@ -360,14 +392,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
-      tc::fence_before_sync();
+      fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
+      tc::fence_before_sync();   // P stores in TMEM before the arrival
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kPFull);
+      if (lane == 0) mbar_arrive(bars + kPFull + sb);
     }
 
-    // ---- O / l for this row
-    mbar_wait(bars + kPvDone, (nkv - 1) & 1, p.err);
+    // ---- O / l for this row, after the last P V
+    mbar_wait(bars + kPvDone + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, p.err);
     tc::fence_after_sync();
     const float inv = 1.f / l;
     OutT* dst = reinterpret_cast<OutT*>(p.out) + static_cast<int64_t>(q0 + i0 + tok) * p.o_st +
