@@ -137,7 +137,12 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  * Supported: D in {64, 128}; BS = 16; G = Hq/Hkv in {1, 2, 4, 8}.
  * Work is split along the context in splits of up to 512 tokens (fewer for
  * short tables); for a sequence with more than one split, the last split to
- * finish merges them.  The split scratch is a per-(device, stream) buffer
+ * finish merges them.  Two kernels compute the same result: a two-pass one
+ * per split (logits staged in shared memory; the default) and a single-pass
+ * online-softmax one, selected for the process by the environment variable
+ * FORGE_DECODE_KERNEL=online (read at each call), which is faster on
+ * batches of very uneven lengths.  Every decode entry point of this header
+ * uses the same selection.  The split scratch is a per-(device, stream) buffer
  * that the library allocates with cudaMalloc (and zero-fills) on first need
  * and keeps, growing it when a larger problem arrives; the first call of a
  * given size on a stream should therefore come before any stream capture.

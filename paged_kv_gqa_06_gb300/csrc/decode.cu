@@ -37,6 +37,8 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -678,6 +680,423 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   if (tid == 0) *counter = 0;  // ready for the next call
 }
 
+// ---------------------------------------------------------------------------
+// Single-pass variant: online softmax per block.
+//
+// The two-pass kernel above keeps every logit of a split in shared memory and
+// stops streaming while it takes the split's softmax.  This one carries K and
+// V of the same blocks in each stage (one block per consumer warp) and keeps,
+// per warp and head, a running maximum and sum: per block it computes the
+// 16 x G logits on the tensor cores, moves the maximum (rescaling that warp's
+// O accumulators when it grows), and adds P V at once.  No logits buffer and
+// no split-wide barrier: the ring streams without a pause and more of the
+// shared memory holds data in flight.  The two warps' states are merged at
+// the end (common maximum, rescaled sums), then the output or the split's
+// partial is written exactly as above.
+struct OnlineLayout {
+  size_t ring, pscr, red_ml, bars, total;
+};
+
+// ring (1024-aligned; a stage is [K warp 0 | K warp 1 | V warp 0 | V warp 1],
+// reused at the end for the consumer-warp merge) | per-warp P scratch
+// [8 heads][16 tokens] fp32 | per-warp (max, sum) | mbarriers.
+__host__ __device__ inline OnlineLayout online_layout(int D, int G, int nstage) {
+  OnlineLayout l;
+  size_t off = 1024;
+  l.ring = off;
+  const size_t ring = static_cast<size_t>(nstage) * kStageBlocks * 2 * kBlockSize * D * 2;
+  const size_t red = static_cast<size_t>(kConsumerWarps) * G * D * 4;
+  off += ring > red ? ring : red;
+  l.pscr = off;
+  off += static_cast<size_t>(kConsumerWarps) * 8 * kBlockSize * 4;
+  l.red_ml = off;
+  off += static_cast<size_t>(2) * kConsumerWarps * G * 4;
+  off = (off + 15) & ~static_cast<size_t>(15);
+  l.bars = off;
+  off += static_cast<size_t>(2) * nstage * 8;
+  l.total = off;
+  return l;
+}
+
+template <int D, int G, typename OutT>
+__global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                           const __grid_constant__ CUtensorMap tmv,
+                                                                           const DecodeParams p) {
+  constexpr int TILE_BYTES = kBlockSize * D * 2;
+  constexpr int BOXES = D / kBoxDims;
+  constexpr int KSTEPS = D / 16;
+  static_assert(D % kBoxDims == 0 && G >= 1 && G <= 8, "shape not built");
+
+  const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
+  const int nblk = (L + kBlockSize - 1) / kBlockSize;
+  const int nsplit = (nblk + p.bps - 1) / p.bps;
+
+  if (L == 0) {  // empty context: the output is defined as zero
+    if (s == 0) {
+      for (int o = threadIdx.x; o < G * D; o += kThreads) {
+        const int i = o / D, d = o % D;
+        store_out(reinterpret_cast<OutT*>(p.out) + b * p.o_sb + (g * G + i) * p.o_sh + d, 0.f);
+      }
+    }
+    return;
+  }
+  if (s >= nsplit) return;
+
+  const int blk0 = s * p.bps;
+  const int n = min(p.bps, nblk - blk0);                  // KV blocks in this split (>= 1)
+  const int nst = (n + kStageBlocks - 1) / kStageBlocks;  // stages (K and V of 2 blocks each)
+  const int nstage = p.nstage;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const OnlineLayout lay = online_layout(D, G, nstage);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t ring_s = (sbase + static_cast<uint32_t>(lay.ring)) & ~1023u;
+  unsigned char* ring = smem + (ring_s - sbase);
+  float* red = reinterpret_cast<float*>(ring);  // consumer-warp merge, after the last stage
+  float* pscr = reinterpret_cast<float*>(smem + lay.pscr);
+  float* red_m = reinterpret_cast<float*>(smem + lay.red_ml);
+  float* red_l = red_m + kConsumerWarps * G;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  uint64_t* empty = full + nstage;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nstage; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0;
+    const int e0 = lane < n ? __ldg(row + lane) : 0;
+    const int e1 = lane + 32 < n ? __ldg(row + 32 + lane) : 0;
+    const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
+                     (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int st = 0; st < nst; ++st) {
+      int pb[kStageBlocks];
+#pragma unroll
+      for (int u = 0; u < kStageBlocks; ++u) {
+        const int j = st * kStageBlocks + u;  // <= 64
+        pb[u] = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
+        if (j >= n) pb[u] = -1;  // past the split: no tile
+      }
+      if (lane == 0) {
+        if (st >= nstage) mbar_wait(empty + slot, phase ^ 1u, p.err);  // stage released
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int u = 0; u < kStageBlocks; ++u)
+          if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += 2 * TILE_BYTES;
+        if (bytes) {
+          mbar_arrive_expect_tx(full + slot, bytes);
+#pragma unroll
+          for (int u = 0; u < kStageBlocks; ++u) {
+            if (static_cast<unsigned>(pb[u]) >= static_cast<unsigned>(p.NB)) continue;
+            unsigned char* kt = ring + (slot * 2 * kStageBlocks + u) * TILE_BYTES;
+            unsigned char* vt = ring + (slot * 2 * kStageBlocks + kStageBlocks + u) * TILE_BYTES;
+#pragma unroll
+            for (int c = 0; c < BOXES; ++c) {
+              tma_load_4d(kt + c * kBoxBytes, &tmk, c * kBoxDims, 0, g, pb[u], full + slot);
+              tma_load_4d(vt + c * kBoxBytes, &tmv, c * kBoxDims, 0, g, pb[u], full + slot);
+            }
+          }
+        } else {
+          mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
+        }
+      }
+      if (++slot == nstage) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    return;
+  }
+
+
+  // -------------------------------------------------------------- consumers
+  const int tid = threadIdx.x;  // 0 .. kConsumers-1
+  const int tq = lane >> 2;     // MMA group id: a token (QK) / a dim (PV) row, and the head of B
+  const int tr = lane & 3;      // MMA thread-in-group: a pair of columns
+  const int t_base = blk0 * kBlockSize;
+
+  // B operand of QK^T, q^T (k = dim, n = head), for all KSTEPS; heads >= G are 0.
+  // The optional q/k path runs at position L-1 (the new token's).
+  const int pos = L - 1;
+  const bool qk_path = p.q_norm_w != nullptr || p.k_norm_w != nullptr || p.rope != nullptr;
+  const bool rope = p.rope != nullptr && pos < p.rope_rows;
+  if (p.rope != nullptr && !rope && tid == 0 && s == 0 && g == 0) record_error(p.err, kDevErrPosition);
+  uint32_t qb[KSTEPS][2];
+  {
+    const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + tq) * p.q_sh;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      qb[ks][0] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
+      qb[ks][1] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
+    }
+    if (qk_path) {  // uniform across the CTA
+      float x[KSTEPS][4];
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        x[ks][0] = bf16lo(qb[ks][0]);
+        x[ks][1] = bf16hi(qb[ks][0]);
+        x[ks][2] = bf16lo(qb[ks][1]);
+        x[ks][3] = bf16hi(qb[ks][1]);
+      }
+      q_norm_rope<D>(x, tr, p, pos, rope);
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        qb[ks][0] = tq < G ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
+        qb[ks][1] = tq < G ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
+      }
+    }
+  }
+
+  // Fused append: the split holding position L-1 patches that row of its last
+  // block with this step's new K (before QK^T) and V (before P V), and stores it.
+  const bool fused = p.k_new != nullptr && s == nsplit - 1;
+  const int jl = n - 1, rl = (L - 1) % kBlockSize;  // block within the split, row
+  __nv_bfloat16* kdst = nullptr;
+  __nv_bfloat16* vdst = nullptr;
+  if (fused) {
+    const int pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0 + jl);
+    if (static_cast<unsigned>(pb) < static_cast<unsigned>(p.NB)) {  // a bad id is recorded by the producer
+      kdst = p.k_cache_w + static_cast<int64_t>(pb) * p.kc_sblk + g * p.kc_sh + rl * D;
+      vdst = p.v_cache_w + static_cast<int64_t>(pb) * p.vc_sblk + g * p.vc_sh + rl * D;
+    }
+  }
+
+  // Running state of this warp for heads h0 = 2 tr, h1 = 2 tr + 1 (the S and
+  // O accumulator columns this thread holds): maximum (log2 units) and this
+  // lane's part of the sum; O^T (dims x heads) accumulators.
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[KSTEPS][4];
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float* psc = pscr + warp * 8 * kBlockSize;  // this warp's P^T scratch [head][token]
+
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int st = 0; st < nst; ++st) {
+    mbar_wait(full + slot, phase, p.err);
+    const int j = st * kStageBlocks + warp;  // block within the split
+    if (j < n) {
+      unsigned char* kt = ring + (slot * 2 * kStageBlocks + warp) * TILE_BYTES;
+      unsigned char* vt = ring + (slot * 2 * kStageBlocks + kStageBlocks + warp) * TILE_BYTES;
+      const uint32_t kt_s = ring_s + (slot * 2 * kStageBlocks + warp) * TILE_BYTES;
+      const uint32_t vt_s = ring_s + (slot * 2 * kStageBlocks + kStageBlocks + warp) * TILE_BYTES;
+      if (fused && j == jl) {
+        const __nv_bfloat16* src = p.k_new + static_cast<int64_t>(b) * p.kn_sb + g * p.kn_sh;
+        if (qk_path)
+          patch_new_k_row<D>(kt, src, kdst, rl, lane, p, pos, rope);
+        else
+          patch_new_row<D>(kt, src, kdst, rl, lane);
+      }
+      // ---- S^T = K q^T: 16 tokens x 8 heads
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;  // token row this lane addresses
+        const int acol = lane >> 4;                           // +0 / +1 chunk
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(swz(kt_s, arow, 2 * ks + acol), a);
+          if (ks & 1)
+            mma_16816_bf16(c1, a, qb[ks][0], qb[ks][1]);
+          else
+            mma_16816_bf16(c0, a, qb[ks][0], qb[ks][1]);
+        }
+      }
+      const int tpos = t_base + j * kBlockSize;
+      const bool v0 = tpos + tq < L, v1 = tpos + tq + 8 < L;
+      const float s00 = v0 ? (c0[0] + c1[0]) * p.qk_scale_log2 : -INFINITY;  // token tq, head h0
+      const float s01 = v0 ? (c0[1] + c1[1]) * p.qk_scale_log2 : -INFINITY;  // token tq, head h1
+      const float s10 = v1 ? (c0[2] + c1[2]) * p.qk_scale_log2 : -INFINITY;  // token tq + 8, head h0
+      const float s11 = v1 ? (c0[3] + c1[3]) * p.qk_scale_log2 : -INFINITY;  // token tq + 8, head h1
+      // the block's maximum per head: over the 8 lanes sharing tr (every block
+      // of the split holds at least one token of the sequence, so it is finite)
+      float mt0 = fmaxf(s00, s10), mt1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
+      }
+      const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
+      const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);  // 0 on the first block
+      m0 = mn0;
+      m1 = mn1;
+      const float p00 = fast_exp2(s00 - mn0), p01 = fast_exp2(s01 - mn1);
+      const float p10 = fast_exp2(s10 - mn0), p11 = fast_exp2(s11 - mn1);
+      l0 = fmaf(l0, a0, p00 + p10);
+      l1 = fmaf(l1, a1, p01 + p11);
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
+        }
+      }
+      // P^T through the scratch: [head][token]
+      psc[(2 * tr) * kBlockSize + tq] = p00;
+      psc[(2 * tr + 1) * kBlockSize + tq] = p01;
+      psc[(2 * tr) * kBlockSize + tq + 8] = p10;
+      psc[(2 * tr + 1) * kBlockSize + tq + 8] = p11;
+      const int live = L - tpos;  // >= 1 tokens of this block are in the sequence
+      if (live < kBlockSize) {
+        // the sequence ends inside this block: zero the V rows past its end
+        // (they may hold anything, NaN included; P is 0 there but 0*NaN is NaN)
+        for (int idx = lane; idx < (kBlockSize - live) * BOXES * 8; idx += 32) {
+          const int r = live + idx / (BOXES * 8), rest = idx % (BOXES * 8);
+          *reinterpret_cast<uint4*>(vt + (rest >> 3) * kBoxBytes + r * 128 + (rest & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // before the TMA engine refills this stage
+      }
+      __syncwarp();
+      if (fused && j == jl)
+        patch_new_row<D>(vt, p.v_new + static_cast<int64_t>(b) * p.vn_sb + g * p.vn_sh, vdst, rl, lane);
+      // ---- O^T += V^T P^T, P as bf16 high + low parts
+      uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
+      if (tq < G) {
+        const float2 pa = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 2 * tr);
+        const float2 pc = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 8 + 2 * tr);
+        split_bf16x2(pa.x, pa.y, bh0, bl0);
+        split_bf16x2(pc.x, pc.y, bh1, bl1);
+      }
+      {
+        const int arow = (lane & 7) + (lane >> 4) * 8;  // token row this lane addresses
+        const int acol = (lane >> 3) & 1;               // +0 / +1 chunk
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_trans(swz(vt_s, arow, 2 * mt + acol), a);
+          mma_16816_bf16(o[mt], a, bh0, bh1);
+          mma_16816_bf16(o[mt], a, bl0, bl1);
+        }
+      }
+    }
+    __syncwarp();  // the scratch is rewritten by the next block
+    if (lane == 0) mbar_arrive(empty + slot);
+    if (++slot == nstage) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+
+
+  // ---- merge the two warps' states: per head, the common maximum M; each
+  // warp's O and sum scaled by 2^(m_w - M) (0 for a warp that had no block)
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  const int h0 = 2 * tr, h1 = 2 * tr + 1;
+  named_barrier(1, kConsumers);  // both warps are done with the ring; it is reused below
+  if (tq == 0) {
+    if (h0 < G) red_m[warp * G + h0] = m0;
+    if (h1 < G) red_m[warp * G + h1] = m1;
+  }
+  named_barrier(1, kConsumers);
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    if (h0 < G) M0 = fmaxf(M0, red_m[w * G + h0]);
+    if (h1 < G) M1 = fmaxf(M1, red_m[w * G + h1]);
+  }
+  const float f0 = h0 < G ? fast_exp2(m0 - M0) : 0.f, f1 = h1 < G ? fast_exp2(m1 - M1) : 0.f;
+  if (tq == 0) {
+    if (h0 < G) red_l[warp * G + h0] = l0 * f0;
+    if (h1 < G) red_l[warp * G + h1] = l1 * f1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt) {
+    const int d0 = 16 * mt + tq, d1 = d0 + 8;
+    if (h0 < G) {
+      red[(warp * G + h0) * D + d0] = o[mt][0] * f0;
+      red[(warp * G + h0) * D + d1] = o[mt][2] * f0;
+    }
+    if (h1 < G) {
+      red[(warp * G + h1) * D + d0] = o[mt][1] * f1;
+      red[(warp * G + h1) * D + d1] = o[mt][3] * f1;
+    }
+  }
+  named_barrier(1, kConsumers);
+
+  for (int o4 = tid * 4; o4 < G * D; o4 += kConsumers * 4) {
+    const int i = o4 / D, d = o4 % D;
+    float4 t = *reinterpret_cast<const float4*>(red + i * D + d);
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(red + (w * G + i) * D + d);
+      t.x += x.x;
+      t.y += x.y;
+      t.z += x.z;
+      t.w += x.w;
+    }
+    float li = red_l[i];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) li += red_l[w * G + i];
+    const int h = g * G + i;
+    if (nsplit == 1) {
+      OutT* dst = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + h * p.o_sh + d;
+      store_out(dst + 0, t.x / li);
+      store_out(dst + 1, t.y / li);
+      store_out(dst + 2, t.z / li);
+      store_out(dst + 3, t.w / li);
+    } else {
+      *reinterpret_cast<float4*>(p.ws_acc + ((static_cast<int64_t>(b) * p.Hq + h) * p.s_max + s) * D + d) = t;
+    }
+  }
+  if (nsplit == 1) return;
+  if (tid < G) {
+    float mi = red_m[tid], li = red_l[tid];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      mi = fmaxf(mi, red_m[w * G + tid]);
+      li += red_l[w * G + tid];
+    }
+    const int64_t r = (static_cast<int64_t>(b) * p.Hq + g * G + tid) * p.s_max + s;
+    p.ws_ml[2 * r] = mi;
+    p.ws_ml[2 * r + 1] = li;
+  }
+
+  // ---- split reduce by the last CTA of (b, g) to arrive
+  __threadfence();  // this thread's partial stores, device-wide, before the arrival
+  named_barrier(1, kConsumers);
+  int* counter = p.counters + static_cast<int64_t>(b) * p.Hkv + g;
+  if (tid == 0) red_m[0] = __int_as_float(atomicAdd(counter, 1) == nsplit - 1 ? 1 : 0);
+  named_barrier(1, kConsumers);
+  if (__float_as_int(red_m[0]) == 0) return;
+  __threadfence();  // every other split's partial is now visible; read it past L1
+  const size_t ring_bytes = lay.pscr - lay.ring;
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red, static_cast<int>(ring_bytes / (4 * G)), red_m, red_l);
+  if (tid == 0) *counter = 0;  // ready for the next call
+}
+
+
+// Which decode kernel: the two-pass one unless FORGE_DECODE_KERNEL=online.
+bool decode_online() {
+  const char* e = std::getenv("FORGE_DECODE_KERNEL");
+  return e && std::strcmp(e, "online") == 0;
+}
+
+// Ring depth of the single-pass kernel: 3 stages (its fastest setting on
+// every measured workload) unless FORGE_PAGED_NSTAGE chose one for both.
+int online_nstage(int requested) {
+  static const bool chosen = std::getenv("FORGE_PAGED_NSTAGE") != nullptr;
+  return chosen ? requested : 3;
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device and size.
 // `set_for` is the caller's own per-kernel record of what it already set.
 template <typename K>
@@ -700,12 +1119,23 @@ cudaError_t ensure_smem(K kernel, size_t bytes, std::atomic<size_t> (&set_for)[6
 template <int D, int G, typename OutT>
 cudaError_t launch_typed(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.Hkv), static_cast<unsigned>(p.B), static_cast<unsigned>(p.s_max));
+  if (decode_online()) {
+    DecodeParams po = p;
+    po.nstage = online_nstage(p.nstage);
+    const size_t smem = online_layout(D, G, po.nstage).total;
+    auto kernel = paged_gqa_decode_online_kernel<D, G, OutT>;
+    static std::atomic<size_t> smem_set[64];  // one record per instantiation
+    cudaError_t e = ensure_smem(kernel, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, po);
+    return cudaGetLastError();
+  }
   const size_t smem = decode_layout(D, G, p.bps, p.nstage).total;
   auto split_kernel = paged_gqa_decode_split_kernel<D, G, OutT>;
   static std::atomic<size_t> smem_set[64];  // one record per instantiation
   cudaError_t e = ensure_smem(split_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(p.Hkv), static_cast<unsigned>(p.B), static_cast<unsigned>(p.s_max));
   split_kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
   return cudaGetLastError();
 }

@@ -17,3 +17,14 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(params=["two_pass", "online"])
+def decode_kernel(request, monkeypatch):
+    """Both decode kernels behind every decode entry point: the two-pass split
+    kernel (default) and the single-pass online-softmax one."""
+    if request.param == "online":
+        monkeypatch.setenv("FORGE_DECODE_KERNEL", "online")
+    else:
+        monkeypatch.delenv("FORGE_DECODE_KERNEL", raising=False)
+    return request.param

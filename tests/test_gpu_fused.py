@@ -9,7 +9,7 @@ from gpu_util import (DEV, TOL, DeviceLayer, assert_device_clean, bits_host, max
 from paged_kv_gqa_06_gb300 import binding
 from paged_kv_gqa_06_gb300 import workloads as W
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("decode_kernel")]
 
 
 @pytest.fixture(scope="module", autouse=True)

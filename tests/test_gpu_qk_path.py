@@ -17,7 +17,7 @@ from gpu_util import DEV, TOL, DeviceLayer, bits_host, max_abs_err, out_tensor
 from paged_kv_gqa_06_gb300 import binding
 from paged_kv_gqa_06_gb300 import workloads as W
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("decode_kernel")]
 
 THETA = 1e6   # Qwen3's rotary base
 EPS = 1e-6

@@ -19,7 +19,7 @@ from gpu_util import TOL, DeviceLayer, max_abs_err, oracle_appended, oracle_deco
 from paged_kv_gqa_06_gb300 import binding
 from paged_kv_gqa_06_gb300 import workloads as W
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("decode_kernel")]
 
 
 @pytest.fixture(scope="module", autouse=True)
