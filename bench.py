@@ -65,10 +65,14 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
 
 
-def _traffic_from_profile(src_hash: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode source; else None."""
-    p = os.path.join(ROOT, "profiles", "decode_split_qwen3_4b.md")
+DECODE_KERNELS = {"online": "paged_gqa_decode_online_kernel", "two_pass": "paged_gqa_decode_split_kernel"}
+PROFILE_FILES = {"online": "decode_online_qwen3_4b.md", "two_pass": "decode_split_qwen3_4b.md"}
+
+
+def _traffic_from_profile(src_hash: str, kernel: str):
+    """DRAM bytes per Qwen3-4B decode launch of `kernel` from its committed ncu
+    summary, if that was taken on the current decode source; else None."""
+    p = os.path.join(ROOT, "profiles", PROFILE_FILES[kernel])
     if not os.path.exists(p):
         return None
     vals = {}
@@ -521,7 +525,8 @@ def run_native(args, wl, out_bytes):
     value = aggregate_gbs(ws, bytes_step, args.steps, ms_total)
     dec_avg_ms = statistics.fmean(decode_ms)
     achieved = bytes_layer / (dec_avg_ms * 1e-3) / 1e9
-    traffic = _traffic_from_profile(_decode_source_hash())
+    split_tokens, kern = binding.forge_paged_gqa_decode_plan(wl.B, wl.Hkv, wl.MB)
+    traffic = _traffic_from_profile(_decode_source_hash(), kern) if wl.spec.name == "qwen3_4b" else None
     h2d = total  # the packed input buffer, as copied each step
     d2h = host_out.numel() * host_out.element_size()
     line = {
@@ -536,9 +541,10 @@ def run_native(args, wl, out_bytes):
                                     "layers": L, "bytes_per_step": bytes_step,
                                     "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged_gqa_decode_split_kernel (one decode call; split merge inside)"
+                     "kernel": (f"{DECODE_KERNELS[kern]} (one decode call; split merge inside)"
                                 if args.path == "separate" else
-                                "paged_gqa_decode_split_kernel with fused append (one launch per layer)"),
+                                f"{DECODE_KERNELS[kern]} with fused append (one launch per layer)"),
+                     "split_tokens": split_tokens,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),

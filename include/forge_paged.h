@@ -138,11 +138,10 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  * Work is split along the context in splits of up to 512 tokens (fewer for
  * short tables); for a sequence with more than one split, the last split to
  * finish merges them.  Two kernels compute the same result: a two-pass one
- * per split (logits staged in shared memory; the default) and a single-pass
- * online-softmax one, selected for the process by the environment variable
- * FORGE_DECODE_KERNEL=online (read at each call), which is faster on
- * batches of very uneven lengths.  Every decode entry point of this header
- * uses the same selection.  The split scratch is a per-(device, stream) buffer
+ * per split (logits staged in shared memory) and a single-pass
+ * online-softmax one; forge_paged_gqa_decode_plan states which one a call
+ * uses and how long its splits are.  Every decode entry point of this header
+ * uses the same choice.  The split scratch is a per-(device, stream) buffer
  * that the library allocates with cudaMalloc (and zero-fills) on first need
  * and keeps, growing it when a larger problem arrives; the first call of a
  * given size on a stream should therefore come before any stream capture.
@@ -163,6 +162,26 @@ FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *
  */
 FORGE_API size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
                                               int max_blocks_per_seq, int split_tokens);
+
+/* Decode kernels a plan can choose (forge_paged_gqa_decode_plan). */
+#define FORGE_DECODE_TWO_PASS 0 /* logits of a split staged in shared memory, then P V */
+#define FORGE_DECODE_ONLINE 1   /* single pass, running max and sum per head */
+
+/*
+ * The split length and kernel that the decode entry points use for these
+ * sizes on a GPU with num_sms SMs (num_sms > 0).  split_tokens as for
+ * forge_paged_gqa_decode_ex (0 = automatic).  Automatic length: the longest
+ * split from 1024 tokens, halving down to 64, whose upper bound on CTAs
+ * (B * Hkv * ceil(max_blocks_per_seq * 16 / split)) reaches 4 * num_sms.
+ * Kernel: FORGE_DECODE_ONLINE for splits of 512 tokens or more, else
+ * FORGE_DECODE_TWO_PASS (an automatic two-pass split is at most 512 tokens);
+ * the environment variable FORGE_DECODE_KERNEL ("online" / "two_pass")
+ * overrides the kernel.  Writes *split_tokens_out and *kernel_out; returns
+ * FORGE_OK, FORGE_ERR_NULL, FORGE_ERR_VALUE (bad split_tokens or num_sms) or
+ * FORGE_ERR_SHAPE (negative sizes).  Host-only, no CUDA call.
+ */
+FORGE_API int forge_paged_gqa_decode_plan(int B, int Hkv, int max_blocks_per_seq, int split_tokens,
+                                          int num_sms, int *split_tokens_out, int *kernel_out);
 
 /*
  * forge_paged_gqa_decode_ex -- forge_paged_gqa_decode with caller-owned

@@ -31,6 +31,7 @@ __all__ = [
     "forge_paged_gqa_decode_noalloc",
     "forge_paged_prefill",
     "forge_paged_gqa_decode_workspace_bytes",
+    "forge_paged_gqa_decode_plan",
     "forge_paged_get_device_error",
     "forge_kv_pool_create",
     "forge_kv_pool_destroy",

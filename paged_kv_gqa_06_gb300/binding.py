@@ -92,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.forge_paged_gqa_decode_noalloc.restype = ctypes.c_int
         lib.forge_paged_gqa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 6
         lib.forge_paged_gqa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.forge_paged_gqa_decode_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)] * 2
+        lib.forge_paged_gqa_decode_plan.restype = ctypes.c_int
         lib.forge_status_string.argtypes = [ctypes.c_int]
         lib.forge_status_string.restype = ctypes.c_char_p
         lib.forge_paged_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -240,6 +242,22 @@ def forge_paged_gqa_decode_noalloc(q, k_cache, v_cache, block_tables, context_le
 def forge_paged_gqa_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks_per_seq, split_tokens=0) -> int:
     return int(load_library().forge_paged_gqa_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks_per_seq,
                                                                       split_tokens))
+
+
+FORGE_DECODE_TWO_PASS, FORGE_DECODE_ONLINE = 0, 1
+DECODE_KERNEL_NAMES = {FORGE_DECODE_TWO_PASS: "two_pass", FORGE_DECODE_ONLINE: "online"}
+
+
+def forge_paged_gqa_decode_plan(B, Hkv, max_blocks_per_seq, split_tokens=0, num_sms=None):
+    """(split length in tokens, kernel name) that decode calls of these sizes
+    use; num_sms defaults to the current CUDA device's SM count."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    st, kern = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load_library().forge_paged_gqa_decode_plan(B, Hkv, max_blocks_per_seq, split_tokens, num_sms,
+                                                    ctypes.byref(st), ctypes.byref(kern))
+    _raise(rc, "forge_paged_gqa_decode_plan")
+    return st.value, DECODE_KERNEL_NAMES[kern.value]
 
 
 def forge_paged_gqa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out,

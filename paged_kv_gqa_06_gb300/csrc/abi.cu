@@ -3,6 +3,7 @@
 // Host side only: argument validation, split planning from host-known shapes
 // (no device reads, so calls stay asynchronous and capturable), the split
 // workspace cache, the device error word, and the kernel launches.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -24,7 +25,8 @@ using forge::kBlockSize;
 __device__ int g_device_error;
 
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultSplitTokens = 512;
+constexpr int kDefaultSplitTokens = 512;     // longest automatic split of the two-pass kernel
+constexpr int kOnlineMinSplitTokens = 512;   // automatic kernel choice: single-pass from here up
 constexpr int kMaxSplitTokens = 1024;  // producer lanes hold <= 64 table entries
 constexpr int kMinSplitTokens = 16;
 
@@ -172,20 +174,46 @@ bool prefill_use_mma_sync() {
   return e && std::strcmp(e, "mma") == 0;
 }
 
-int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms) {
-  if (split_tokens > 0) return split_tokens / kBlockSize;
-  // Automatic: 512-token splits, shortened while the upper bound on CTAs
-  // (every sequence as long as its table row) would not give ~4 CTAs per SM.
-  // Shorter splits than that add more merge work than parallelism (measured:
-  // Qwen3-0.6B-shaped batch of 8, 12.8 us at 128-token splits against 16.0 us
-  // at 64).
-  int bps = kDefaultSplitTokens / kBlockSize;
-  const int64_t want = 4ll * (num_sms > 0 ? num_sms : 148);
-  while (bps > 4) {
-    const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((MB + bps - 1) / bps);
-    if (ctas >= want) break;
-    bps /= 2;
+// Decode kernel forced by FORGE_DECODE_KERNEL ("online" or "two_pass"), read
+// at every call; 0 when unset (the plan chooses).
+int decode_kernel_forced() {
+  const char* e = std::getenv("FORGE_DECODE_KERNEL");
+  if (!e) return 0;
+  if (std::strcmp(e, "online") == 0) return 2;
+  if (std::strcmp(e, "two_pass") == 0) return 1;
+  return 0;
+}
+
+// Split length (KV blocks) and decode kernel of a call.
+//
+// Automatic length: the longest split, from 1024 tokens halving down to 64,
+// whose upper bound on CTAs (every sequence as long as its table row) gives
+// ~4 CTAs per SM.  Shorter splits than that add more merge work than
+// parallelism (measured: Qwen3-0.6B-shaped batch of 8, 12.8 us at 128-token
+// splits against 16.0 us at 64).
+//
+// Kernel: splits of 512 tokens or more run the single-pass online-softmax
+// kernel, whose shared memory is all K/V ring (more bytes in flight per SM);
+// shorter ones the two-pass kernel, whose small logits buffer leaves room for
+// 8 CTAs per SM.  Measured on GB300, decode of one layer: Qwen3-4B-shaped
+// batch of 32, 93.6 us single-pass at 1024 tokens against 97.9 us two-pass at
+// 512; Qwen3-0.6B-shaped batch of 8, 11.7 us two-pass at 128 tokens against
+// 14.9 us single-pass.  FORGE_DECODE_KERNEL overrides the kernel.
+int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms, int* online) {
+  int bps = kMaxSplitTokens / kBlockSize;
+  if (split_tokens > 0) {
+    bps = split_tokens / kBlockSize;
+  } else {
+    const int64_t want = 4ll * (num_sms > 0 ? num_sms : 148);
+    while (bps > 4) {
+      const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((MB + bps - 1) / bps);
+      if (ctas >= want) break;
+      bps /= 2;
+    }
   }
+  const int forced = decode_kernel_forced();
+  *online = forced ? (forced == 2) : (bps * kBlockSize >= kOnlineMinSplitTokens);
+  if (split_tokens == 0 && !*online) bps = std::min(bps, kDefaultSplitTokens / kBlockSize);
   return bps;
 }
 
@@ -207,13 +235,16 @@ size_t workspace_bytes_for(int64_t B, int64_t Hq, int64_t D, int64_t s_max) {
   return kCounterBytes + round256(acc) + ml;
 }
 
-int nstage_default() {
+// Ring depth: 2 stages for the two-pass kernel, 3 for the single-pass one
+// (each kernel's fastest setting on the measured workloads), unless
+// FORGE_PAGED_NSTAGE sets one for both.
+int nstage_for(bool online) {
   static int v = [] {
     const char* e = std::getenv("FORGE_PAGED_NSTAGE");
     int n = e ? std::atoi(e) : 0;
-    return (n >= 2 && n <= 16) ? n : 2;
+    return (n >= 2 && n <= 16) ? n : 0;
   }();
-  return v;
+  return v ? v : (online ? 3 : 2);
 }
 
 int plan_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_tensor* v_cache,
@@ -281,10 +312,10 @@ int plan_decode(const forge_tensor* q, const forge_tensor* k_cache, const forge_
   p.Hkv = static_cast<int>(Hkv);
   p.NB = static_cast<int>(NB);
   p.MB = static_cast<int>(MB);
-  p.bps = split_blocks_for(split_tokens, p.B, p.Hkv, p.MB, num_sms);
+  p.bps = split_blocks_for(split_tokens, p.B, p.Hkv, p.MB, num_sms, &p.online);
   p.s_max = MB > 0 ? static_cast<int>((MB + p.bps - 1) / p.bps) : 1;
   if (p.s_max > 65535) return FORGE_ERR_UNSUPPORTED;  // grid z limit
-  p.nstage = nstage_default();
+  p.nstage = nstage_for(p.online != 0);
   p.qk_scale_log2 = scale * 1.4426950408889634f;
   plan->ws_bytes = workspace_bytes_for(B, Hq, D, p.s_max);
   if (plan->ws_bytes > 0 && B * Hkv > kCounterSlots) return FORGE_ERR_UNSUPPORTED;
@@ -391,6 +422,21 @@ int forge_paged_kv_append(const forge_tensor* k_new, const forge_tensor* v_new,
   p.NB = static_cast<int>(k_cache->shape[0]);
   p.err = err;
   if (forge::launch_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FORGE_ERR_CUDA;
+  return FORGE_OK;
+}
+
+int forge_paged_gqa_decode_plan(int B, int Hkv, int max_blocks_per_seq, int split_tokens, int num_sms,
+                                int* split_tokens_out, int* kernel_out) {
+  if (!split_tokens_out || !kernel_out) return FORGE_ERR_NULL;
+  if (B < 0 || Hkv <= 0 || max_blocks_per_seq < 0) return FORGE_ERR_SHAPE;
+  if (num_sms <= 0) return FORGE_ERR_VALUE;
+  if (split_tokens != 0 &&
+      (split_tokens < kMinSplitTokens || split_tokens > kMaxSplitTokens || split_tokens % kBlockSize != 0))
+    return FORGE_ERR_VALUE;
+  int online = 0;
+  const int bps = split_blocks_for(split_tokens, B, Hkv, max_blocks_per_seq, num_sms, &online);
+  *split_tokens_out = bps * kBlockSize;
+  *kernel_out = online ? FORGE_DECODE_ONLINE : FORGE_DECODE_TWO_PASS;
   return FORGE_OK;
 }
 

@@ -58,6 +58,7 @@ struct DecodeParams {
   int bps;         // KV blocks per split
   int s_max;       // split slots per (b, h) in the workspace
   int nstage;      // shared-memory ring depth (pipeline stages)
+  int online;      // 1: single-pass online-softmax kernel; 0: two-pass kernel
   float qk_scale_log2;  // scale * log2(e): logits come out in log2 units
   // Fused append (all null for a plain decode): the new K/V row of sequence
   // b, KV head g, written at position L_b - 1 of the cache before use.

@@ -37,8 +37,6 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
-#include <cstdlib>
-#include <cstring>
 
 #include "common.cuh"
 
@@ -82,6 +80,14 @@ __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __fl
 
 // Clamp a sequence length to what its block-table row can address; record a
 // device error when the caller broke that precondition.
+// A read-only load the compiler keeps where it is written (it is not sunk
+// below the early exits that follow it), so that it overlaps other loads.
+__device__ __forceinline__ int ld_nc_keep(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
 __device__ __forceinline__ int checked_length(const DecodeParams& p, int b, bool report) {
   int L = __ldg(p.context_lens + b);
   const int Lmax = p.MB * kBlockSize;
@@ -210,111 +216,115 @@ __device__ __forceinline__ void patch_new_k_row(unsigned char* tile, const __nv_
 
 // Split reduce for the G heads of (b, g): with M = max_s m_s and
 // w_s = 2^(m_s - M), out = sum_s w_s acc_s / sum_s w_s l_s over the nsplit
-// partials in the workspace.  Run by the kConsumers threads of the last CTA:
-// the max and the denominator are reduced cooperatively, the weights of a
-// chunk of up to `wcap` splits are staged in shared memory (`wbuf`,
-// [G][wcap]), and each thread accumulates 4 consecutive dims of outputs with
-// 8 partial rows in flight.  Workspace reads bypass L1 (other SMs wrote them).
+// partials in the workspace.  Run by the kConsumers threads of the last CTA.
+// Each L2 round trip here sits on the kernel's tail, so the reads are issued
+// together: per chunk of up to wcap / (2 G) splits (`wbuf` holds wcap
+// floats), the first U partial rows of every output this thread owns are
+// requested, then the chunk's (m, l) pairs are copied to shared memory
+// ([G][chunk] float2) while those rows are in flight.  Each thread then takes its heads' maximum over the chunk
+// from shared memory and accumulates 4 consecutive dims per output; a
+// running maximum carries across chunks (the sums are rescaled when it
+// grows).  Workspace reads bypass L1 (other SMs wrote them).
 template <int D, int G, typename OutT>
 __device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int g, int nsplit, int tid, float* wbuf,
-                                             int wcap, float* red_m, float* red_l) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int64_t row0 = static_cast<int64_t>(b) * p.Hq + g * G;  // first head of the group
-  float M[G], den[G];
+                                             int wcap) {
+  constexpr int kOut = (G * D / 4 + kConsumers - 1) / kConsumers;  // float4 outputs per thread
+  constexpr int U = kOut >= 4 ? 1 : 8 / kOut;                      // partial rows in flight per output
+  const int64_t row0 = static_cast<int64_t>(b) * p.Hq + g * G;    // first head of the group
+  const int cap = wcap / (2 * G);  // splits per chunk
+  float2* mlb = reinterpret_cast<float2*>(wbuf);
+  const float2* ws_ml = reinterpret_cast<const float2*>(p.ws_ml);
+
+  constexpr bool kEven = (G * D / 4) % kConsumers == 0;  // every thread owns kOut outputs
+  // output k of this thread: head (k * kConsumers + tid) / (D / 4), dims 4 * ((...) % (D / 4))
+  auto valid = [&](int k) { return kEven || (tid + k * kConsumers) * 4 < G * D; };
+  auto head = [&](int k) { return valid(k) ? (tid + k * kConsumers) * 4 / D : 0; };
+  auto acc = [&](int k, int sp) {
+    const int o4 = valid(k) ? (tid + k * kConsumers) * 4 : 0;
+    return reinterpret_cast<const float4*>(p.ws_acc + ((row0 + o4 / D) * p.s_max + sp) * D + o4 % D);
+  };
+  float4 num[kOut];
+  float M[kOut], den[kOut];
 #pragma unroll
-  for (int i = 0; i < G; ++i) {
-    const float* ml = p.ws_ml + (row0 + i) * p.s_max * 2;
-    float mx = -INFINITY;
-    for (int s = tid; s < nsplit; s += kConsumers) mx = fmaxf(mx, __ldcg(ml + 2 * s));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red_m[warp * G + i] = mx;
-  }
-  named_barrier(1, kConsumers);
-#pragma unroll
-  for (int i = 0; i < G; ++i) {
-    M[i] = red_m[i];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) M[i] = fmaxf(M[i], red_m[w * G + i]);
-    const float* ml = p.ws_ml + (row0 + i) * p.s_max * 2;
-    float dn = 0.f;
-    for (int s = tid; s < nsplit; s += kConsumers) dn += fast_exp2(__ldcg(ml + 2 * s) - M[i]) * __ldcg(ml + 2 * s + 1);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dn += __shfl_xor_sync(0xffffffffu, dn, off);
-    if (lane == 0) red_l[warp * G + i] = dn;
-  }
-  named_barrier(1, kConsumers);
-#pragma unroll
-  for (int i = 0; i < G; ++i) {
-    den[i] = red_l[i];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) den[i] += red_l[w * G + i];
+  for (int k = 0; k < kOut; ++k) {
+    num[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    M[k] = -INFINITY;
+    den[k] = 0.f;
   }
 
-  constexpr int kOut = (G * D / 4 + kConsumers - 1) / kConsumers;  // float4 outputs per thread
-  constexpr int U = 8;
-  float4 num[kOut];
+  for (int s0 = 0; s0 < nsplit; s0 += cap) {
+    const int cnt = min(cap, nsplit - s0);
+    float4 x[kOut][U];
 #pragma unroll
-  for (int k = 0; k < kOut; ++k) num[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < nsplit; s0 += wcap) {
-    const int cnt = min(wcap, nsplit - s0);
+    for (int k = 0; k < kOut; ++k)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        x[k][u] = valid(k) && u < cnt ? __ldcg(acc(k, s0 + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int idx = tid; idx < G * cnt; idx += kConsumers) {
-      const int i = idx / cnt, sl = idx % cnt;
-      float Mi = M[0];
-#pragma unroll
-      for (int k = 1; k < G; ++k)
-        if (i == k) Mi = M[k];
-      wbuf[i * wcap + sl] = fast_exp2(__ldcg(p.ws_ml + ((row0 + i) * p.s_max + s0 + sl) * 2) - Mi);
+      const int i = idx / cnt, sl = idx - i * cnt;
+      mlb[i * cap + sl] = __ldcg(ws_ml + (row0 + i) * p.s_max + s0 + sl);
     }
     named_barrier(1, kConsumers);
 #pragma unroll
     for (int k = 0; k < kOut; ++k) {
-      const int o4 = (tid + k * kConsumers) * 4;
-      if (o4 < G * D) {
-        const int i = o4 / D, d = o4 % D;
-        const float* acc = p.ws_acc + ((row0 + i) * p.s_max + s0) * D + d;
-        const float* w = wbuf + i * wcap;
-        float4 n = num[k];
-        for (int sl = 0; sl < cnt; sl += U) {
-          float4 x[U];
+      if (!valid(k)) continue;
+      const float2* mk = mlb + head(k) * cap;
+      float mc = M[k];
+      for (int sl = 0; sl < cnt; ++sl) mc = fmaxf(mc, mk[sl].x);
+      const float sc = fast_exp2(M[k] - mc);  // 0 on the first chunk
+      num[k].x *= sc;
+      num[k].y *= sc;
+      num[k].z *= sc;
+      num[k].w *= sc;
+      den[k] *= sc;
+      M[k] = mc;
+    }
+    for (int sl = 0; sl < cnt; sl += U) {
+      if (sl > 0) {
+#pragma unroll
+        for (int k = 0; k < kOut; ++k)
 #pragma unroll
           for (int u = 0; u < U; ++u)
-            x[u] = sl + u < cnt ? __ldcg(reinterpret_cast<const float4*>(acc + static_cast<int64_t>(sl + u) * D))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[k][u] = valid(k) && sl + u < cnt ? __ldcg(acc(k, s0 + sl + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const float wu = sl + u < cnt ? w[sl + u] : 0.f;
-            n.x = fmaf(wu, x[u].x, n.x);
-            n.y = fmaf(wu, x[u].y, n.y);
-            n.z = fmaf(wu, x[u].z, n.z);
-            n.w = fmaf(wu, x[u].w, n.w);
-          }
+      for (int k = 0; k < kOut; ++k) {
+        if (!valid(k)) continue;
+        const float2* mk = mlb + head(k) * cap + sl;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (sl + u >= cnt) break;
+          const float2 ml = mk[u];
+          const float w = fast_exp2(ml.x - M[k]);
+          num[k].x = fmaf(w, x[k][u].x, num[k].x);
+          num[k].y = fmaf(w, x[k][u].y, num[k].y);
+          num[k].z = fmaf(w, x[k][u].z, num[k].z);
+          num[k].w = fmaf(w, x[k][u].w, num[k].w);
+          den[k] = fmaf(w, ml.y, den[k]);
         }
-        num[k] = n;
       }
     }
     named_barrier(1, kConsumers);  // wbuf is rewritten by the next chunk
   }
 #pragma unroll
   for (int k = 0; k < kOut; ++k) {
-    const int o4 = (tid + k * kConsumers) * 4;
-    if (o4 < G * D) {
-      const int i = o4 / D, d = o4 % D;
-      float dn = den[0];
-#pragma unroll
-      for (int j = 1; j < G; ++j)
-        if (i == j) dn = den[j];
-      OutT* dst = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + (g * G + i) * p.o_sh + d;
-      store_out(dst + 0, num[k].x / dn);
-      store_out(dst + 1, num[k].y / dn);
-      store_out(dst + 2, num[k].z / dn);
-      store_out(dst + 3, num[k].w / dn);
-    }
+    if (!valid(k)) continue;
+    const int d = (tid + k * kConsumers) * 4 % D;
+    OutT* dst = reinterpret_cast<OutT*>(p.out) + b * p.o_sb + (g * G + head(k)) * p.o_sh + d;
+    store_out(dst + 0, num[k].x / den[k]);
+    store_out(dst + 1, num[k].y / den[k]);
+    store_out(dst + 2, num[k].z / den[k]);
+    store_out(dst + 3, num[k].w / den[k]);
   }
 }
 
+// Minimum resident CTAs the register budget must allow: what shared memory
+// allows at the default split length and ring depth (8 for G <= 4, 6 for G = 8).
+template <int G>
+constexpr int split_min_blocks() { return G <= 4 ? 8 : 6; }
+
 template <int D, int G, typename OutT>
-__global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                           const __grid_constant__ CUtensorMap tmv,
                                                                           const DecodeParams p) {
   constexpr int TILE_BYTES = kBlockSize * D * 2;
@@ -327,6 +337,16 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // The producer's block-table entries for this split are requested with the
+  // length, not after it (entries past the sequence are loaded but unused;
+  // the row has MB entries).
+  int e0 = 0, e1 = 0;
+  if (warp == kConsumerWarps) {
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
+    const int room = min(p.bps, p.MB - s * p.bps);
+    if (lane < room) e0 = ld_nc_keep(row + lane);
+    if (lane + 32 < room) e1 = ld_nc_keep(row + 32 + lane);
+  }
   const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
   const int nblk = (L + kBlockSize - 1) / kBlockSize;
   const int nsplit = (nblk + p.bps - 1) / p.bps;
@@ -371,9 +391,6 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0;
-    const int e0 = lane < n ? __ldg(row + lane) : 0;
-    const int e1 = lane + 32 < n ? __ldg(row + 32 + lane) : 0;
     const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
                      (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
     if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
@@ -676,7 +693,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_split_kernel(const 
   named_barrier(1, kConsumers);
   if (__float_as_int(red_m[0]) == 0) return;
   __threadfence();  // every other split's partial is now visible; read it past L1
-  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, logits, lrow, red_m, red_l);
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, logits, G * lrow);
   if (tid == 0) *counter = 0;  // ready for the next call
 }
 
@@ -730,6 +747,16 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // The producer's block-table entries for this split are requested with the
+  // length, not after it (entries past the sequence are loaded but unused;
+  // the row has MB entries).
+  int e0 = 0, e1 = 0;
+  if (warp == kConsumerWarps) {
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
+    const int room = min(p.bps, p.MB - s * p.bps);
+    if (lane < room) e0 = ld_nc_keep(row + lane);
+    if (lane + 32 < room) e1 = ld_nc_keep(row + 32 + lane);
+  }
   const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
   const int nblk = (L + kBlockSize - 1) / kBlockSize;
   const int nsplit = (nblk + p.bps - 1) / p.bps;
@@ -773,9 +800,6 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0;
-    const int e0 = lane < n ? __ldg(row + lane) : 0;
-    const int e1 = lane + 32 < n ? __ldg(row + 32 + lane) : 0;
     const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
                      (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
     if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
@@ -1079,23 +1103,10 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   if (__float_as_int(red_m[0]) == 0) return;
   __threadfence();  // every other split's partial is now visible; read it past L1
   const size_t ring_bytes = lay.pscr - lay.ring;
-  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red, static_cast<int>(ring_bytes / (4 * G)), red_m, red_l);
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red, static_cast<int>(ring_bytes / 4));
   if (tid == 0) *counter = 0;  // ready for the next call
 }
 
-
-// Which decode kernel: the two-pass one unless FORGE_DECODE_KERNEL=online.
-bool decode_online() {
-  const char* e = std::getenv("FORGE_DECODE_KERNEL");
-  return e && std::strcmp(e, "online") == 0;
-}
-
-// Ring depth of the single-pass kernel: 3 stages (its fastest setting on
-// every measured workload) unless FORGE_PAGED_NSTAGE chose one for both.
-int online_nstage(int requested) {
-  static const bool chosen = std::getenv("FORGE_PAGED_NSTAGE") != nullptr;
-  return chosen ? requested : 3;
-}
 
 // Raise a kernel's dynamic shared-memory limit once per device and size.
 // `set_for` is the caller's own per-kernel record of what it already set.
@@ -1120,15 +1131,13 @@ template <int D, int G, typename OutT>
 cudaError_t launch_typed(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.Hkv), static_cast<unsigned>(p.B), static_cast<unsigned>(p.s_max));
-  if (decode_online()) {
-    DecodeParams po = p;
-    po.nstage = online_nstage(p.nstage);
-    const size_t smem = online_layout(D, G, po.nstage).total;
+  if (p.online) {
+    const size_t smem = online_layout(D, G, p.nstage).total;
     auto kernel = paged_gqa_decode_online_kernel<D, G, OutT>;
     static std::atomic<size_t> smem_set[64];  // one record per instantiation
     cudaError_t e = ensure_smem(kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, po);
+    kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
     return cudaGetLastError();
   }
   const size_t smem = decode_layout(D, G, p.bps, p.nstage).total;

@@ -21,10 +21,8 @@ def oracle_mod():
 
 @pytest.fixture(params=["two_pass", "online"])
 def decode_kernel(request, monkeypatch):
-    """Both decode kernels behind every decode entry point: the two-pass split
-    kernel (default) and the single-pass online-softmax one."""
-    if request.param == "online":
-        monkeypatch.setenv("FORGE_DECODE_KERNEL", "online")
-    else:
-        monkeypatch.delenv("FORGE_DECODE_KERNEL", raising=False)
+    """Both decode kernels behind every decode entry point, each forced: the
+    two-pass split kernel and the single-pass online-softmax one (the library
+    otherwise picks one per call from the split length)."""
+    monkeypatch.setenv("FORGE_DECODE_KERNEL", request.param)
     return request.param
