@@ -342,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   // the row has MB entries).
   int e0 = 0, e1 = 0;
   if (warp == kConsumerWarps) {
+    if (lane == 0) {  // the TMA descriptors, fetched while the length and table are read
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
     const int room = min(p.bps, p.MB - s * p.bps);
     if (lane < room) e0 = ld_nc_keep(row + lane);
@@ -686,13 +690,20 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   }
 
   // ---- split reduce by the last CTA of (b, g) to arrive
-  __threadfence();  // this thread's partial stores, device-wide, before the arrival
+  // Arrival: the barrier orders every consumer's partial stores before thread
+  // 0's fence and atomic (release); in the last CTA, thread 0's second fence
+  // and the barrier order the other splits' partials before every thread's
+  // reads (acquire) -- the pattern of a grid-wide barrier.
   named_barrier(1, kConsumers);
   int* counter = p.counters + static_cast<int64_t>(b) * p.Hkv + g;
-  if (tid == 0) red_m[0] = __int_as_float(atomicAdd(counter, 1) == nsplit - 1 ? 1 : 0);
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(counter, 1) == nsplit - 1;
+    if (last) __threadfence();
+    red_m[0] = __int_as_float(last ? 1 : 0);
+  }
   named_barrier(1, kConsumers);
   if (__float_as_int(red_m[0]) == 0) return;
-  __threadfence();  // every other split's partial is now visible; read it past L1
   merge_splits<D, G, OutT>(p, b, g, nsplit, tid, logits, G * lrow);
   if (tid == 0) *counter = 0;  // ready for the next call
 }
@@ -752,6 +763,10 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   // the row has MB entries).
   int e0 = 0, e1 = 0;
   if (warp == kConsumerWarps) {
+    if (lane == 0) {  // the TMA descriptors, fetched while the length and table are read
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
     const int room = min(p.bps, p.MB - s * p.bps);
     if (lane < room) e0 = ld_nc_keep(row + lane);
@@ -1095,13 +1110,20 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   }
 
   // ---- split reduce by the last CTA of (b, g) to arrive
-  __threadfence();  // this thread's partial stores, device-wide, before the arrival
+  // Arrival: the barrier orders every consumer's partial stores before thread
+  // 0's fence and atomic (release); in the last CTA, thread 0's second fence
+  // and the barrier order the other splits' partials before every thread's
+  // reads (acquire) -- the pattern of a grid-wide barrier.
   named_barrier(1, kConsumers);
   int* counter = p.counters + static_cast<int64_t>(b) * p.Hkv + g;
-  if (tid == 0) red_m[0] = __int_as_float(atomicAdd(counter, 1) == nsplit - 1 ? 1 : 0);
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(counter, 1) == nsplit - 1;
+    if (last) __threadfence();
+    red_m[0] = __int_as_float(last ? 1 : 0);
+  }
   named_barrier(1, kConsumers);
   if (__float_as_int(red_m[0]) == 0) return;
-  __threadfence();  // every other split's partial is now visible; read it past L1
   const size_t ring_bytes = lay.pscr - lay.ring;
   merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red, static_cast<int>(ring_bytes / 4));
   if (tid == 0) *counter = 0;  // ready for the next call
