@@ -810,7 +810,10 @@ def run_prefill(args, name):
                    "flops_rule": "4 * D * Hq per (query token, attended token)",
                    "step": "forge_paged_kv_append of the run's K/V + forge_paged_prefill, CUDA graph",
                    "l2": f"{copies} cache copies rotated ({copies * kv_bytes / 1e6:.0f} MB of K/V vs 126 MB L2)"},
-        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)"
+                                if os.environ.get("FORGE_PREFILL_KERNEL") == "mma" else
+                                "paged_prefill_tc_kernel (tcgen05.mma, accumulators in TMEM, P from TMEM)"),
                      "achieved": round(tflops_kernel, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(tflops_kernel / peak, 4), "traffic": None,
                      "prefill_us": round(ms_kernel * 1e3, 2), "peak_source": peak_src},
