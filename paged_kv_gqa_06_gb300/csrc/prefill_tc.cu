@@ -12,28 +12,30 @@
 //   * warp 4 (producer) loads the Q tile once (a 3-D TMA box of 64 dims x G
 //     heads x 128/G tokens, which lands as 128 K-major rows) and streams the
 //     sequence's K and V, 64 tokens (4 blocks) per stage, through the block
-//     table into a 2-stage ring, up to the tile's last query position;
-//   * warp 5 (MMA) owns 256 TMEM columns: S in two 64-column buffers and the
-//     output accumulator O (D columns).  Its lane 0 issues S_j = Q K_j^T
-//     (M 128, N 64, K = D; Q and K K-major straight from the TMA layout) and
-//     O += P_j V_j (M 128, N = D, K 64; P read from TMEM, where the softmax
-//     wrote it over its S buffer; V MN-major as it lies in the stage), each
-//     as soon as its inputs are ready, so the tensor cores compute S of the
-//     next tile while the softmax works on this one; tcgen05.commit on
-//     mbarriers tracks completion and frees stages and buffers;
+//     table into a 3-stage ring, up to the tile's last query position.  The
+//     third stage is the Q tile's own space, filled once Q is in TMEM;
 //   * warps 0-3 (softmax) own one row each (warp w reads TMEM lanes
-//     32w..32w+31).  Per tile: load the row of S, mask by position (only on
-//     tiles that reach past the row's position), and keep a running maximum
-//     that only moves when the row's maximum grows by more than 8 in log2
-//     units, so the weights stay <= 2^8 and O in TMEM is rescaled rarely.
-//     The weights P = 2^(scale s - m) are stored over the row's S in TMEM,
-//     two per column in the buffer's first 32 columns.  For fp32 output they
-//     are split into bf16 high and low parts (low in the next 32 columns; two
-//     MMAs keep ~16 bits of each weight, as in the decode); for bf16 output
-//     they are rounded to bf16 once (relative error 2^-9, below the output's
-//     own rounding) and P V takes one MMA per K step.  The softmax waits on
-//     the tensor cores only when O has to be rescaled.  At the end O is
-//     divided by the row sum and stored.
+//     32w..32w+31).  First each thread copies its row of Q from shared memory
+//     into TMEM, where it is the A operand of every QK^T.  Per tile: load the
+//     row of S, mask by position (only on tiles that reach past the row's
+//     position), and keep a running maximum that only moves when the row's
+//     maximum grows by more than 8 in log2 units, so the weights stay <= 2^8
+//     and O in TMEM is rescaled rarely.  The weights P = 2^(scale s - m) are
+//     stored over the row's S in TMEM, two per column in its first 32
+//     columns.  For fp32 output they are split into bf16 high and low parts
+//     (low in the next 32 columns; two MMAs keep ~16 bits of each weight, as
+//     in the decode); for bf16 output they are rounded to bf16 once (relative
+//     error 2^-9, below the output's own rounding) and P V takes one MMA per K
+//     step.  At the end O is divided by the row sum and stored;
+//   * warp 5 (MMA) owns 256 TMEM columns: S (64), Q (D / 2: two bf16 per
+//     column) and the output accumulator O (D).  Its lane 0 issues
+//     S_j = Q K_j^T (M 128, N 64, K = D; Q from TMEM, K K-major straight from
+//     the TMA layout) and O += P_j V_j (M 128, N = D, K 64; P from TMEM over
+//     S, V MN-major as it lies in the stage), each as soon as its inputs are
+//     ready: S_{j+1} overwrites S, so it waits for P_j V_j.  tcgen05.commit on
+//     mbarriers tracks completion and frees stages.  With Q in TMEM, QK^T
+//     reads only K from shared memory: on this GPU an MMA with both operands
+//     in shared memory runs at well under the rate of one with A in TMEM.
 // Shared memory is 98 KB and TMEM 256 columns per CTA, so two CTAs share an
 // SM: while one CTA's softmax runs, the other's MMAs keep the tensor cores
 // busy.
@@ -52,11 +54,13 @@ namespace {
 
 constexpr int kTcRows = 128;                 // MMA M
 constexpr int kTcKv = 64;                    // tokens per stage (MMA N of S, K of P V)
-constexpr int kTcStages = 2;                 // K/V ring depth
+constexpr int kTcStages = 3;                 // K/V ring depth: 2 stages + the Q tile's space once Q is in TMEM
 constexpr int kTcThreads = 6 * 32;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kTmemCols = 256;
-constexpr int kColO = 128;                   // O columns start here; S buffers at 0 and 64
+constexpr int kColS = 0;                     // S (and P over it): 64 columns
+constexpr int kColQ = 64;                    // Q, the A operand of QK^T: D / 2 columns (2 bf16 each)
+constexpr int kColO = 128;                   // O: D columns
 constexpr float kRescaleSlack = 8.0f;        // log2 units: weights stay <= 2^8
 constexpr unsigned kFullMask = 0xffffffffu;
 
@@ -64,16 +68,23 @@ struct TcLayout {
   int q, kv, bars, total;
 };
 
-// Q [BOXES][128 rows][128 B] | kTcStages x ([K: BOXES][64][128 B], [V: same]) |
-// mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.
+// Q [BOXES][128 rows][128 B] | 2 x ([K: BOXES][64][128 B], [V: same]) |
+// mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.  The third
+// K/V stage uses Q's space once Q has been copied into TMEM.
 __host__ __device__ constexpr TcLayout tc_layout(int D) {
   const int boxes = D / 64;
   TcLayout l{};
   l.q = 0;
   l.kv = l.q + boxes * kTcRows * 128;
-  l.bars = l.kv + kTcStages * 2 * boxes * kTcKv * 128;
+  l.bars = l.kv + 2 * 2 * boxes * kTcKv * 128;  // stages 0 and 1; stage 2 reuses Q's space
   l.total = l.bars + 16 * 8 + 1024;          // barriers + slot, + alignment slack
   return l;
+}
+
+// Shared-memory offset of K/V stage st: two stages after Q, the third in
+// Q's own space (free once Q has been copied into TMEM; same size as a stage).
+__host__ __device__ constexpr int stage_offset(const TcLayout& l, int st, int stage_bytes) {
+  return st < 2 ? l.kv + st * stage_bytes : l.q;
 }
 
 // mbarrier slots
@@ -84,7 +95,8 @@ constexpr int kSFull = kKvEmpty + kTcStages; // [2]: S_j written
 constexpr int kPFull = kSFull + 2;           // [2]: P_j written over S_j
 constexpr int kPvDone = kPFull + 2;          // [2]: P_j V_j done, S/P buffer free
 constexpr int kDrain = kPvDone + 2;
-constexpr int kSlot = kDrain + 1;            // TMEM address (4 bytes) after the barriers
+constexpr int kQTmem = kDrain + 1;           // Q copied into TMEM (one arrival per softmax warp)
+constexpr int kSlot = kQTmem + 1;            // TMEM address (4 bytes) after the barriers
 
 // 32 consecutive outputs of a row: fp32 accumulators times `inv`.
 __device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], float inv) {
@@ -198,6 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(bars + kPvDone + i, 1);
     }
     mbar_init(bars + kDrain, 1);
+    mbar_init(bars + kQTmem, 4);
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -219,8 +232,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
       for (int j = 0; j < nkv; ++j) {
         const int st = j % kTcStages, use = j / kTcStages;
-        if (use > 0) mbar_wait(bars + kKvEmpty + st, (use - 1) & 1, p.err);  // stage released by P V
-        unsigned char* kst = sm + lay.kv + st * 2 * KV_HALF;
+        if (use > 0)
+          mbar_wait(bars + kKvEmpty + st, (use - 1) & 1, p.err);  // stage released by P V
+        else if (st == 2)
+          mbar_wait(bars + kQTmem, 0, p.err);  // Q's space: free once Q is in TMEM
+        unsigned char* kst = sm + stage_offset(lay, st, 2 * KV_HALF);
         int pb[4];
         uint32_t bytes = 0;
 #pragma unroll
@@ -261,42 +277,41 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // (P_{j-2} V done); O += P_j V_j needs P_j written.  Waiting for one
     // would hold back the other and stall the ring.
     if (lane == 0) {
-      mbar_wait(bars + kQFull, 0, p.err);
+      mbar_wait(bars + kQTmem, 0, p.err);
       tc::fence_after_sync();
       int next_qk = 0, next_pv = 0;
       uint64_t last = global_timer_ns();
       while (next_pv < nkv) {
         bool progressed = false;
-        if (next_qk < nkv && next_qk <= next_pv + 1) {
-          const int j = next_qk, st = j % kTcStages, sb = j & 1;
+        if (next_qk < nkv && next_qk == next_pv) {  // one S buffer: P_{j-1} V_{j-1} issued first
+          const int j = next_qk, st = j % kTcStages;
           if (mbar_try_wait(bars + kKvFull + st, (j / kTcStages) & 1) &&
-              (j < 2 || mbar_try_wait(bars + kPvDone + sb, ((j >> 1) - 1) & 1))) {
+              (j < 1 || mbar_try_wait(bars + kPvDone, (j - 1) & 1))) {
             tc::fence_after_sync();
-            const uint32_t kst = sm_s + lay.kv + st * 2 * KV_HALF;
+            const uint32_t kst = sm_s + stage_offset(lay, st, 2 * KV_HALF);
 #pragma unroll
             for (int k = 0; k < KSTEPS; ++k) {
-              const uint64_t a = tc::smem_desc_sw128(sm_s + lay.q + (k >> 2) * kTcRows * 128 + (k & 3) * 32, 0, 1024);
               const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
-              tc::mma_bf16_ss(tmem + sb * kTcKv, a, bd, IDESC_S, k > 0);
+              tc::mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * k, bd, IDESC_S, k > 0);
             }
-            tc::commit(smem_addr(bars + kSFull + sb));
+            tc::commit(smem_addr(bars + kSFull));
             ++next_qk;
             progressed = true;
           }
         }
         if (next_pv < next_qk) {
-          const int jp = next_pv, pbuf = jp & 1, stp = jp % kTcStages;
-          if (mbar_try_wait(bars + kPFull + pbuf, (jp >> 1) & 1)) {
+          const int jp = next_pv, stp = jp % kTcStages;
+          if (mbar_try_wait(bars + kPFull, jp & 1)) {
             tc::fence_after_sync();
-            const uint32_t vst = sm_s + lay.kv + stp * 2 * KV_HALF + KV_HALF;
-            const uint32_t phi = tmem + pbuf * kTcKv, plo = phi + kTcKv / 2;  // P over S in TMEM
+            const uint32_t vst = sm_s + stage_offset(lay, stp, 2 * KV_HALF) + KV_HALF;
+            const uint32_t phi = tmem + kColS, plo = phi + kTcKv / 2;  // P over S in TMEM
 #pragma unroll
             for (int kk = 0; kk < kTcKv / 16; ++kk) {
               const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
               tc::mma_bf16_ts(tmem + kColO, phi + 8 * kk, bd, IDESC_O, jp > 0 || kk > 0);
               if (kPLow) tc::mma_bf16_ts(tmem + kColO, plo + 8 * kk, bd, IDESC_O, true);
             }
-            tc::commit(smem_addr(bars + kPvDone + pbuf));
+            tc::commit(smem_addr(bars + kPvDone));
             tc::commit(smem_addr(bars + kKvEmpty + stp));
             ++next_pv;
             progressed = true;
@@ -321,16 +336,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const int lim = ok ? pos0 + tok : p_max;       // causal limit of the row
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float scale = p.qk_scale_log2;
+    // This row of Q into TMEM (the A operand of QK^T): from the TMA tile in
+    // shared memory (128-byte rows, 16-byte chunks swizzled by row % 8), 32
+    // columns of two bf16 per box of 64 dims
+    mbar_wait(bars + kQFull, 0, p.err);
+#pragma unroll
+    for (int c = 0; c < BOXES; ++c) {
+      uint32_t v[32];
+      const unsigned char* qrow = sm + lay.q + c * kTcRows * 128 + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) * 16));
+        v[4 * ch] = w.x;
+        v[4 * ch + 1] = w.y;
+        v[4 * ch + 2] = w.z;
+        v[4 * ch + 3] = w.w;
+      }
+      tc::st_32x32b_x32(trow + kColQ + 32 * c, v);
+    }
+    tc::wait_st();
+    tc::fence_before_sync();
+    fence_proxy_async_smem();  // the Q reads above before the TMA engine refills this space
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kQTmem);
     float m_used = -INFINITY, l = 0.f;             // max the weights are taken against; row sum
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      mbar_wait(bars + kSFull + sb, (j >> 1) & 1, p.err);
+      const int sb = 0;                            // one S buffer at kColS
+      mbar_wait(bars + kSFull, j & 1, p.err);
       tc::fence_after_sync();
       float s[kTcKv];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[32];
-        tc::ld_32x32b_x32(trow + sb * kTcKv + 32 * h, v);
+        tc::ld_32x32b_x32(trow + kColS + 32 * h, v);
         tc::wait_ld();
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[32 * h + c] = __uint_as_float(v[c]);
@@ -354,7 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       if (j >= 1 && __any_sync(kFullMask, need)) {
         // rescale O: every P V so far (the last is tile j-1) must be finished
-        mbar_wait(bars + kPvDone + ((j - 1) & 1), ((j - 1) >> 1) & 1, p.err);
+        mbar_wait(bars + kPvDone, (j - 1) & 1, p.err);
         tc::fence_after_sync();
         const float f = need ? alpha : 1.f;
 #pragma unroll
@@ -385,8 +423,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           else
             hi[e] = pack_bf16x2(a, c);
         }
-        tc::st_32x32b_x16(trow + sb * kTcKv + 16 * h, hi);
-        if (kPLow) tc::st_32x32b_x16(trow + sb * kTcKv + kTcKv / 2 + 16 * h, lo);
+        tc::st_32x32b_x16(trow + kColS + sb + 16 * h, hi);
+        if (kPLow) tc::st_32x32b_x16(trow + kColS + sb + kTcKv / 2 + 16 * h, lo);
       }
       tc::wait_st();
       if (j == nkv - 1) {
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
         const int z0 = min(L - t0, loaded);
         if (z0 < kTcKv) {
-          unsigned char* vst = sm + lay.kv + (j % kTcStages) * 2 * KV_HALF + KV_HALF;
+          unsigned char* vst = sm + stage_offset(lay, j % kTcStages, 2 * KV_HALF) + KV_HALF;
           for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kSoftmaxThreads) {
             const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
             *reinterpret_cast<uint4*>(vst + (rest >> 3) * kTcKv * 128 + vr * 128 + (rest & 7) * 16) =
@@ -405,11 +443,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       tc::fence_before_sync();   // P stores in TMEM before the arrival
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kPFull + sb);
+      if (lane == 0) mbar_arrive(bars + kPFull);
     }
 
     // ---- O / l for this row, after the last P V
-    mbar_wait(bars + kPvDone + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, p.err);
+    mbar_wait(bars + kPvDone, (nkv - 1) & 1, p.err);
     tc::fence_after_sync();
     const float inv = 1.f / l;
     OutT* dst = reinterpret_cast<OutT*>(p.out) + static_cast<int64_t>(q0 + i0 + tok) * p.o_st +
