@@ -379,9 +379,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
         for (int c = 0; c < kTcKv; ++c) s[c] = t0 + c <= lim ? s[c] : -INFINITY;
       }
-      float mx = -INFINITY;
+      // the row's maximum as a tree (6 levels, not a chain of 64)
+      float mt[kTcKv / 2];
 #pragma unroll
-      for (int c = 0; c < kTcKv; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < kTcKv / 2; ++c) mt[c] = fmaxf(s[c], s[c + kTcKv / 2]);
+#pragma unroll
+      for (int w = kTcKv / 4; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int c = 0; c < w; ++c) mt[c] = fmaxf(mt[c], mt[c + w]);
+      }
+      const float mx = mt[0];
       // every row sees token 0 in the first stage, so m_new is finite
       const float m_new = fmaxf(m_used, mx * scale);
       const bool need = m_new > m_used + kRescaleSlack;
