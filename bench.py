@@ -223,7 +223,7 @@ def cpu_baseline(wl, out_bytes, budget_s=12.0):
     per_pass = sum(_seq_bytes(wl, b, out_bytes) for b in all_seqs)
     passes, elapsed = 0, 0.0
     t0 = time.perf_counter()
-    while passes < 1 or (elapsed < budget_s and passes < 20):
+    while passes < 1 or (elapsed < budget_s and passes < 1000):
         _oracle_step(wl, t, kc, vc, all_seqs, threads)
         passes += 1
         elapsed = time.perf_counter() - t0
