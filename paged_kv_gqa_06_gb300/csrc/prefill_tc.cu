@@ -91,10 +91,10 @@ __host__ __device__ constexpr int stage_offset(const TcLayout& l, int st, int st
 constexpr int kQFull = 0;
 constexpr int kKvFull = 1;                   // [kTcStages]
 constexpr int kKvEmpty = kKvFull + kTcStages;
-constexpr int kSFull = kKvEmpty + kTcStages; // [2]: S_j written
-constexpr int kPFull = kSFull + 2;           // [2]: P_j written over S_j
-constexpr int kPvDone = kPFull + 2;          // [2]: P_j V_j done, S/P buffer free
-constexpr int kDrain = kPvDone + 2;
+constexpr int kSFull = kKvEmpty + kTcStages; // S_j written
+constexpr int kPFull = kSFull + 1;           // P_j written over S_j (one arrival per softmax warp)
+constexpr int kPvDone = kPFull + 1;          // P_j V_j done: S free for S_{j+1}
+constexpr int kDrain = kPvDone + 1;
 constexpr int kQTmem = kDrain + 1;           // Q copied into TMEM (one arrival per softmax warp)
 constexpr int kSlot = kQTmem + 1;            // TMEM address (4 bytes) after the barriers
 
@@ -204,11 +204,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(bars + kKvFull + i, 1);
       mbar_init(bars + kKvEmpty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bars + kSFull + i, 1);
-      mbar_init(bars + kPFull + i, 4);   // one arrival per softmax warp
-      mbar_init(bars + kPvDone + i, 1);
-    }
+    mbar_init(bars + kSFull, 1);
+    mbar_init(bars + kPFull, 4);   // one arrival per softmax warp
+    mbar_init(bars + kPvDone, 1);
     mbar_init(bars + kDrain, 1);
     mbar_init(bars + kQTmem, 4);
     fence_barrier_init();
@@ -361,7 +359,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) mbar_arrive(bars + kQTmem);
     float m_used = -INFINITY, l = 0.f;             // max the weights are taken against; row sum
     for (int j = 0; j < nkv; ++j) {
-      const int sb = 0;                            // one S buffer at kColS
       mbar_wait(bars + kSFull, j & 1, p.err);
       tc::fence_after_sync();
       float s[kTcKv];
@@ -430,8 +427,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           else
             hi[e] = pack_bf16x2(a, c);
         }
-        tc::st_32x32b_x16(trow + kColS + sb + 16 * h, hi);
-        if (kPLow) tc::st_32x32b_x16(trow + kColS + sb + kTcKv / 2 + 16 * h, lo);
+        tc::st_32x32b_x16(trow + kColS + 16 * h, hi);
+        if (kPLow) tc::st_32x32b_x16(trow + kColS + kTcKv / 2 + 16 * h, lo);
       }
       tc::wait_st();
       if (j == nkv - 1) {
