@@ -205,3 +205,44 @@ def test_apply_validates_before_touching_cuda():
             B.forge_batch_apply(lib.batch, t, l, s, stream=0)
         assert e.value.status == status
     assert lib.close() == 0
+
+
+def _drive(seed, nb=300, bs=16, rows=16, budget=1024):
+    """Every step's record of one pool + batch driven by a seeded request stream."""
+    stream = W.request_stream(60, seed, prompt_median=150.0, prompt_max=min(64 * bs - 64, nb * bs // 2),
+                              new_max=64, arrivals_per_step=0.8)
+    lib = Lib(nb, bs, 64, rows, budget)
+    records, retired, step = [], 0, 0
+    while retired < len(stream.seq_ids):
+        for req in stream.arriving(step):
+            lib.submit(*req)
+        rec = lib.step()
+        records.append(rec)
+        retired += len(rec["retired"])
+        step += 1
+        assert step < 100000
+    assert lib.close() == 0
+    return records
+
+
+def test_batches_driven_from_threads_match_the_single_threaded_run():
+    # separate pools and batches from separate host threads at once (the
+    # header says every function is thread-safe): no state is shared
+    import threading
+    seeds = [31, 32, 33, 34]
+    want = [_drive(s) for s in seeds]
+    got, errors = [None] * len(seeds), []
+
+    def work(i):
+        try:
+            got[i] = _drive(seeds[i])
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(seeds))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert got == want
