@@ -15,6 +15,8 @@ namespace forge {
 namespace {
 
 __global__ void __launch_bounds__(256) paged_kv_append_kernel(const AppendParams p) {
+  griddep_launch_dependents();
+  griddep_wait();  // the previous grid's writes (e.g. of k_new / v_new) are complete
   const int chunks = p.D >> 3;
   const int64_t rows = static_cast<int64_t>(p.B) * p.Hkv;
   const int64_t total = 2 * rows * chunks;
@@ -52,8 +54,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 65535) blocks = 65535;  // grid-stride loop covers the rest
-  paged_kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(paged_kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, p);
 }
 
 }  // namespace forge

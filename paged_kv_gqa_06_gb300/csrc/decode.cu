@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   // any second split, so each sequence's shorter last split comes late.
   const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();  // no global access before the previous grid in the stream is complete
 
   // The producer's block-table entries for this split are requested with the
   // length, not after it (entries past the sequence are loaded but unused;
@@ -769,6 +771,8 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
 
   const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();  // no global access before the previous grid in the stream is complete
 
   // The producer's block-table entries for this split are requested with the
   // length, not after it (entries past the sequence are loaded but unused;
@@ -1183,16 +1187,14 @@ cudaError_t launch_typed(const DecodeParams& p, const CUtensorMap& tmk, const CU
     static std::atomic<size_t> smem_set[64];  // one record per instantiation
     cudaError_t e = ensure_smem(kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
-    return cudaGetLastError();
+    return launch_pdl(kernel, grid, dim3(kThreads), smem, stream, tmk, tmv, p);
   }
   const size_t smem = decode_layout(D, G, p.bps, p.nstage).total;
   auto split_kernel = paged_gqa_decode_split_kernel<D, G, OutT>;
   static std::atomic<size_t> smem_set[64];  // one record per instantiation
   cudaError_t e = ensure_smem(split_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
-  split_kernel<<<grid, kThreads, smem, stream>>>(tmk, tmv, p);
-  return cudaGetLastError();
+  return launch_pdl(split_kernel, grid, dim3(kThreads), smem, stream, tmk, tmv, p);
 }
 
 template <int D, typename OutT>
