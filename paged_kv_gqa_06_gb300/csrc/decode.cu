@@ -31,6 +31,13 @@
 //     merges the splits of the G heads (the split reduce) and returns the
 //     counter to zero.  Merging in the last CTA, rather than in a second
 //     kernel, keeps the merge off the launch critical path.
+// That is the two-pass kernel.  A second, single-pass kernel on the same grid
+// (further below) carries K and V of the same blocks in each stage and keeps
+// a running maximum and sum instead of a logits buffer, so all of its shared
+// memory is K/V ring.  The host plan (abi.cu) gives splits of 512 tokens or
+// more to the single-pass kernel and shorter ones to the two-pass kernel.
+// Both are launched with programmatic stream serialization and touch no
+// global memory before griddepcontrol.wait.
 // Slots at t >= L never reach the output: their logits are -inf and their V
 // rows are zeroed in shared memory before the PV product, so NaN in unused
 // slots cannot leak in.
