@@ -200,6 +200,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 16 bytes global -> shared, asynchronous, through L2 only (.cg: no L1 copy,
+// so data other SMs wrote and made visible is read as it is in L2).  The
+// copies a thread issued are complete, and visible to that thread, after its
+// cp_async_wait_all.  dst and src 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // One tiled box of a 3-D tensor map into shared memory (as tma_load_4d).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
   asm volatile(

@@ -223,32 +223,38 @@ __device__ __forceinline__ void patch_new_k_row(unsigned char* tile, const __nv_
 
 // Split reduce for the G heads of (b, g): with M = max_s m_s and
 // w_s = 2^(m_s - M), out = sum_s w_s acc_s / sum_s w_s l_s over the nsplit
-// partials in the workspace.  Run by the kConsumers threads of the last CTA.
-// Each L2 round trip here sits on the kernel's tail, so the reads are issued
-// together: per chunk of up to wcap / (2 G) splits (`wbuf` holds wcap
-// floats), the first U partial rows of every output this thread owns are
-// requested, then the chunk's (m, l) pairs are copied to shared memory
-// ([G][chunk] float2) while those rows are in flight.  Each thread then takes its heads' maximum over the chunk
-// from shared memory and accumulates 4 consecutive dims per output; a
-// running maximum carries across chunks (the sums are rescaled when it
-// grows).  Workspace reads bypass L1 (other SMs wrote them).
+// partials in the workspace.  Run by the kConsumers threads of the last CTA,
+// in shared memory the CTA no longer needs (`wbuf`, wcap floats, 16-byte
+// aligned).  Each L2 round trip here sits on the kernel's tail, so a chunk of
+// up to cap splits is fetched at once: every thread copies the partial rows
+// of the outputs it owns (4 consecutive dims each) straight into shared
+// memory with asynchronous copies, all in flight together, while the
+// chunk's (m, l) pairs are read ([G][cap] float2).  Each thread then takes
+// its heads' maximum over the chunk and accumulates its outputs from its own
+// copies; a running maximum carries across chunks (the sums are rescaled
+// when it grows).  Workspace reads bypass L1 (other SMs wrote them).
+// The callers' buffers hold at least 3 splits per chunk: both pass a region
+// that contains the K/V ring, at least 2 stages of 2 K tiles, 128 D bytes,
+// and a split takes (G D + 2 G) * 4 <= 36 D bytes.
 template <int D, int G, typename OutT>
 __device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int g, int nsplit, int tid, float* wbuf,
                                              int wcap) {
-  constexpr int kOut = (G * D / 4 + kConsumers - 1) / kConsumers;  // float4 outputs per thread
-  constexpr int U = kOut >= 4 ? 1 : 8 / kOut;                      // partial rows in flight per output
-  const int64_t row0 = static_cast<int64_t>(b) * p.Hq + g * G;    // first head of the group
-  const int cap = wcap / (2 * G);  // splits per chunk
-  float2* mlb = reinterpret_cast<float2*>(wbuf);
+  constexpr int kRow4 = G * D / 4;                               // float4 outputs of the group
+  constexpr int kOut = (kRow4 + kConsumers - 1) / kConsumers;    // float4 outputs per thread
+  constexpr bool kEven = kRow4 % kConsumers == 0;                // every thread owns kOut outputs
+  const int64_t row0 = static_cast<int64_t>(b) * p.Hq + g * G;  // first head of the group
+  const int cap = wcap / (G * D + 2 * G);                        // splits per chunk
+  float4* rows = reinterpret_cast<float4*>(wbuf);                // [cap][kRow4]
+  float2* mlb = reinterpret_cast<float2*>(wbuf + static_cast<size_t>(cap) * G * D);  // [G][cap]
   const float2* ws_ml = reinterpret_cast<const float2*>(p.ws_ml);
 
-  constexpr bool kEven = (G * D / 4) % kConsumers == 0;  // every thread owns kOut outputs
-  // output k of this thread: head (k * kConsumers + tid) / (D / 4), dims 4 * ((...) % (D / 4))
-  auto valid = [&](int k) { return kEven || (tid + k * kConsumers) * 4 < G * D; };
-  auto head = [&](int k) { return valid(k) ? (tid + k * kConsumers) * 4 / D : 0; };
+  // output k of this thread: float4 o = tid + k * kConsumers of the group,
+  // head o / (D / 4), dims 4 * (o % (D / 4))
+  auto valid = [&](int k) { return kEven || tid + k * kConsumers < kRow4; };
+  auto head = [&](int k) { return (tid + k * kConsumers) / (D / 4); };
   auto acc = [&](int k, int sp) {
-    const int o4 = valid(k) ? (tid + k * kConsumers) * 4 : 0;
-    return reinterpret_cast<const float4*>(p.ws_acc + ((row0 + o4 / D) * p.s_max + sp) * D + o4 % D);
+    const int o4 = (tid + k * kConsumers) * 4;
+    return p.ws_acc + ((row0 + o4 / D) * p.s_max + sp) * D + o4 % D;
   };
   float4 num[kOut];
   float M[kOut], den[kOut];
@@ -261,17 +267,17 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int g
 
   for (int s0 = 0; s0 < nsplit; s0 += cap) {
     const int cnt = min(cap, nsplit - s0);
-    float4 x[kOut][U];
 #pragma unroll
-    for (int k = 0; k < kOut; ++k)
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        x[k][u] = valid(k) && u < cnt ? __ldcg(acc(k, s0 + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kOut; ++k) {
+      if (!valid(k)) continue;
+      for (int sl = 0; sl < cnt; ++sl) cp_async16(rows + sl * kRow4 + tid + k * kConsumers, acc(k, s0 + sl));
+    }
     for (int idx = tid; idx < G * cnt; idx += kConsumers) {
       const int i = idx / cnt, sl = idx - i * cnt;
       mlb[i * cap + sl] = __ldcg(ws_ml + (row0 + i) * p.s_max + s0 + sl);
     }
-    named_barrier(1, kConsumers);
+    cp_async_wait_all();
+    named_barrier(1, kConsumers);  // the pairs, read by other threads
 #pragma unroll
     for (int k = 0; k < kOut; ++k) {
       if (!valid(k)) continue;
@@ -285,33 +291,18 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, int b, int g
       num[k].w *= sc;
       den[k] *= sc;
       M[k] = mc;
-    }
-    for (int sl = 0; sl < cnt; sl += U) {
-      if (sl > 0) {
-#pragma unroll
-        for (int k = 0; k < kOut; ++k)
-#pragma unroll
-          for (int u = 0; u < U; ++u)
-            x[k][u] = valid(k) && sl + u < cnt ? __ldcg(acc(k, s0 + sl + u)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < kOut; ++k) {
-        if (!valid(k)) continue;
-        const float2* mk = mlb + head(k) * cap + sl;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (sl + u >= cnt) break;
-          const float2 ml = mk[u];
-          const float w = fast_exp2(ml.x - M[k]);
-          num[k].x = fmaf(w, x[k][u].x, num[k].x);
-          num[k].y = fmaf(w, x[k][u].y, num[k].y);
-          num[k].z = fmaf(w, x[k][u].z, num[k].z);
-          num[k].w = fmaf(w, x[k][u].w, num[k].w);
-          den[k] = fmaf(w, ml.y, den[k]);
-        }
+      for (int sl = 0; sl < cnt; ++sl) {
+        const float2 ml = mk[sl];
+        const float4 x = rows[sl * kRow4 + tid + k * kConsumers];
+        const float w = fast_exp2(ml.x - M[k]);
+        num[k].x = fmaf(w, x.x, num[k].x);
+        num[k].y = fmaf(w, x.y, num[k].y);
+        num[k].z = fmaf(w, x.z, num[k].z);
+        num[k].w = fmaf(w, x.w, num[k].w);
+        den[k] = fmaf(w, ml.y, den[k]);
       }
     }
-    named_barrier(1, kConsumers);  // wbuf is rewritten by the next chunk
+    named_barrier(1, kConsumers);  // the pairs are rewritten by the next chunk
   }
 #pragma unroll
   for (int k = 0; k < kOut; ++k) {
@@ -725,7 +716,9 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   }
   named_barrier(1, kConsumers);
   if (__float_as_int(red_m[0]) == 0) return;
-  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, logits, G * lrow);
+  // the ring and the logits behind it are free now
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red,
+                           static_cast<int>((reinterpret_cast<unsigned char*>(red_m) - ring) / 4));
   if (tid == 0) *counter = 0;  // ready for the next call
 }
 
@@ -1159,8 +1152,9 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   }
   named_barrier(1, kConsumers);
   if (__float_as_int(red_m[0]) == 0) return;
-  const size_t ring_bytes = lay.pscr - lay.ring;
-  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red, static_cast<int>(ring_bytes / 4));
+  // the ring and the P scratch behind it are free now
+  merge_splits<D, G, OutT>(p, b, g, nsplit, tid, red,
+                           static_cast<int>((reinterpret_cast<unsigned char*>(red_m) - ring) / 4));
   if (tid == 0) *counter = 0;  // ready for the next call
 }
 
