@@ -44,6 +44,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -767,6 +768,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   constexpr int TILE_BYTES = kBlockSize * D * 2;
   constexpr int BOXES = D / kBoxDims;
   constexpr int KSTEPS = D / 16;
+  constexpr bool kPLow = !std::is_same<OutT, __nv_bfloat16>::value;  // P's low part in P V
   static_assert(D % kBoxDims == 0 && G >= 1 && G <= 8, "shape not built");
 
   const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
@@ -1031,13 +1033,21 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
       __syncwarp();
       if (fused && j == jl)
         patch_new_row<D>(vt, p.v_new + static_cast<int64_t>(b) * p.vn_sb + g * p.vn_sh, vdst, rl, lane);
-      // ---- O^T += V^T P^T, P as bf16 high + low parts
+      // ---- O^T += V^T P^T.  For fp32 output P goes in as bf16 high + low
+      // parts (~16 significant bits); for bf16 output it is rounded to bf16
+      // once (relative error 2^-9, no more than the output's own rounding),
+      // which halves the MMAs of this product.
       uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
       if (tq < G) {
         const float2 pa = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 2 * tr);
         const float2 pc = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 8 + 2 * tr);
-        split_bf16x2(pa.x, pa.y, bh0, bl0);
-        split_bf16x2(pc.x, pc.y, bh1, bl1);
+        if (kPLow) {
+          split_bf16x2(pa.x, pa.y, bh0, bl0);
+          split_bf16x2(pc.x, pc.y, bh1, bl1);
+        } else {
+          bh0 = pack_bf16x2(pa.x, pa.y);
+          bh1 = pack_bf16x2(pc.x, pc.y);
+        }
       }
       {
         const int arow = (lane & 7) + (lane >> 4) * 8;  // token row this lane addresses
@@ -1047,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
           uint32_t a[4];
           ldsm_x4_trans(swz(vt_s, arow, 2 * mt + acol), a);
           mma_16816_bf16(o[mt], a, bh0, bh1);
-          mma_16816_bf16(o[mt], a, bl0, bl1);
+          if (kPLow) mma_16816_bf16(o[mt], a, bl0, bl1);
         }
       }
     }
