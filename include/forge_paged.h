@@ -28,8 +28,11 @@
  * enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy default
  * stream) and returns.  No call reads device memory from the host, so calls
  * can be captured in a CUDA graph (see forge_paged_gqa_decode for its
- * workspace note).  Calls never abort, throw or trap: they return a
- * forge_status.  Argument errors are reported before anything is enqueued.
+ * workspace note).  The append and decode kernels are launched with
+ * programmatic stream serialization, so their start-up may overlap the end of
+ * the previous kernel in the stream, but none touches memory before that
+ * kernel has completed: stream order holds as for a plain launch.  Calls
+ * never abort, throw or trap: they return a forge_status.  Argument errors are reported before anything is enqueued.
  * Violations of the device-side preconditions (a block id outside the pool,
  * a length longer than the table row, a slot outside the pool) make the
  * kernels skip the bad access and record an error code that
@@ -135,13 +138,20 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  *   stream         cudaStream_t.
  *
  * Supported: D in {64, 128}; BS = 16; G = Hq/Hkv in {1, 2, 4, 8}.
- * Work is split along the context in splits of up to 512 tokens (fewer for
- * short tables); for a sequence with more than one split, the last split to
- * finish merges them.  Two kernels compute the same result: a two-pass one
- * per split (logits staged in shared memory) and a single-pass
- * online-softmax one; forge_paged_gqa_decode_plan states which one a call
- * uses and how long its splits are.  Every decode entry point of this header
- * uses the same choice.  The split scratch is a per-(device, stream) buffer
+ * Work is split along the context in splits of up to 1024 tokens (shorter
+ * when B * Hkv is small against the SM count); for a sequence with more than
+ * one split, the last split to finish merges them.  Two kernels compute the
+ * same result: a two-pass one per split (logits staged in shared memory) and
+ * a single-pass online-softmax one; forge_paged_gqa_decode_plan states which
+ * one a call uses and how long its splits are.  Every decode entry point of
+ * this header uses the same choice.
+ * Arithmetic: products of bf16 values on the tensor cores with fp32
+ * accumulation; softmax, sums and the split merge in fp32.  The softmax
+ * weights enter the P V product as bf16 high + low parts (about 16
+ * significant bits) for f32 output; with bf16 output the single-pass kernel
+ * rounds them to bf16 once (relative error 2^-9).  The parity tests hold the
+ * result within 2e-3 (f32 out) or 1.6e-2 (bf16 out) max-abs of exact
+ * attention, for values of the size of N(0, 1) inputs (|V| < 8).  The split scratch is a per-(device, stream) buffer
  * that the library allocates with cudaMalloc (and zero-fills) on first need
  * and keeps, growing it when a larger problem arrives; the first call of a
  * given size on a stream should therefore come before any stream capture.
