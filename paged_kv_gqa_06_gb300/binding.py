@@ -114,7 +114,9 @@ def describe(t: torch.Tensor | None) -> ForgeTensor | None:
 
     Descriptors are cached by (address, dtype, shape, strides): a decode loop
     passes the same tensors every step, and filling a ctypes struct costs
-    more host time than the lookup.  The C side only reads them.
+    more host time than the lookup.  The C side only reads them.  A tensor
+    must be on the current CUDA device (checked when its descriptor is
+    made); ValueError otherwise.
     """
     if t is None:
         return None
@@ -124,6 +126,13 @@ def describe(t: torch.Tensor | None) -> ForgeTensor | None:
         return d
     if t.dim() > 4:
         raise ValueError("forge tensors have at most 4 dims")
+    # The kernels dereference these pointers on the device: a host tensor
+    # would be a memory fault there, not an error status, so it stops here.
+    if not t.is_cuda:
+        raise ValueError(f"forge tensors are CUDA device memory; got a tensor on {t.device}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if len(_desc_cache) >= _DESC_CACHE_MAX:
         _desc_cache.clear()
     d = ForgeTensor()

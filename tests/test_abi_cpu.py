@@ -145,13 +145,22 @@ def test_append_rejects_bad_arguments(lib, over, status):
 
 
 def test_python_binding_raises_on_bad_status(lib):
-    q = torch.zeros(2, 8, 96, dtype=torch.bfloat16)
-    kc = torch.zeros(4, 2, 16, 96, dtype=torch.bfloat16)
-    out = torch.zeros(2, 8, 96)
     with pytest.raises(binding.ForgeError) as e:
+        binding._raise(-4, "forge_paged_gqa_decode")
+    assert e.value.status == -4
+    assert "forge_paged_gqa_decode" in str(e.value)
+    binding._raise(binding.FORGE_OK, "no error")  # no exception
+
+
+def test_python_binding_refuses_host_tensors(lib):
+    # a host pointer would reach the kernels as a device address: refused
+    # before the C call
+    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
+    out = torch.zeros(2, 8, 64)
+    with pytest.raises(ValueError, match="CUDA device memory"):
         binding.forge_paged_gqa_decode(q, kc, kc, torch.zeros(2, 4, dtype=torch.int32),
                                        torch.zeros(2, dtype=torch.int32), 0.1, out, stream=0)
-    assert e.value.status == -4
 
 
 def test_fused_entry_rejects_bad_new_rows(lib):

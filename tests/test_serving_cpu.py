@@ -7,6 +7,7 @@ block), its events (admitted, retired, preempted) and its report must equal
 the oracle's (oracle/serving.py) exactly, on the hand-worked traces and on
 seeded random request streams, including pools small enough to preempt.
 """
+import ctypes
 import json
 import os
 
@@ -200,10 +201,20 @@ def test_apply_validates_before_touching_cuda():
         (tables.t().contiguous().t(), lens, slots, -3),                 # inner stride not 1
         (tables, torch.zeros(8, dtype=torch.int32)[::2], slots, -3),    # strided lengths
     ]
+    def desc(t):  # a descriptor of a host tensor, straight to the C ABI (the binding refuses host tensors)
+        d = B.ForgeTensor()
+        d.data, d.dtype, d.ndim = t.data_ptr(), B._DTYPES[t.dtype], t.dim()
+        for i in range(t.dim()):
+            d.shape[i], d.stride[i] = t.shape[i], t.stride(i)
+        return d
+
     for t, l, s, status in bad:
-        with pytest.raises(B.ForgeError) as e:
-            B.forge_batch_apply(lib.batch, t, l, s, stream=0)
-        assert e.value.status == status
+        dt, dl, ds = desc(t), desc(l), desc(s)
+        rc = B.load_library().forge_batch_apply(lib.batch, ctypes.byref(dt), ctypes.byref(dl), ctypes.byref(ds),
+                                                None)
+        assert rc == status
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        B.forge_batch_apply(lib.batch, tables, lens, slots, stream=0)
     assert lib.close() == 0
 
 
