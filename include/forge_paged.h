@@ -156,7 +156,11 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  * and keeps, growing it when a larger problem arrives; the first call of a
  * given size on a stream should therefore come before any stream capture.
  * Use forge_paged_gqa_decode_ex to pass caller-owned scratch instead.
- * Thread-safe.
+ * Thread-safe for calls on different streams.  Calls from several host
+ * threads on ONE stream must be ordered by the caller: growing that stream's
+ * scratch frees the old buffer once the stream's queued work is done, and a
+ * call that fetched the old buffer but had not yet enqueued its kernel would
+ * then use freed memory.
  */
 FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *k_cache,
                            const forge_tensor *v_cache, const forge_tensor *block_tables,
