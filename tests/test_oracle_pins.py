@@ -6,7 +6,8 @@
 * torch's scaled_dot_product_attention in fp64 (a library routine);
 * closed forms: one token returns its V; equal keys or scale 0 give the mean
   of V; a dominant key returns its V; all-ones V gives ones;
-* invariants: block placement, group isolation, NaN poison, threading.
+* invariants: block placement, group isolation, linearity in V, NaN poison,
+  threading.
 
 The attention definition these follow: "Make the Engine Talk" section 1.3
 (grouped-query attention) and the forge-engine README "What it implements"
@@ -206,6 +207,27 @@ def test_all_ones_values_give_ones(oracle_mod):
     vc = np.where(vc == W.BF16_NAN, vc, _bits(1.0)).astype(np.uint16)
     out = _decode(oracle_mod, wl, t, kc, vc)
     np.testing.assert_allclose(out, 1.0, rtol=0, atol=1e-14)
+
+
+def test_output_is_linear_in_values(oracle_mod):
+    # For a fixed q and K the softmax weights do not depend on V, so
+    # out(a V1 + b V2) = a out(V1) + b out(V2).  Small integers keep every
+    # combination exact in bf16, which leaves only fp64 rounding.
+    wl, t = _small(B=3, Hq=8, Hkv=2, D=64, fixed_lens=(7, 33, 64))
+    kc, vc = _appended(oracle_mod, wl, t)
+    live = vc != W.BF16_NAN
+    rng = np.random.default_rng(11)
+    v1 = rng.integers(-4, 5, size=vc.shape).astype(np.float32)
+    v2 = rng.integers(-4, 5, size=vc.shape).astype(np.float32)
+
+    def cache_of(x):
+        return np.where(live, _bits(x), vc).astype(np.uint16)
+
+    o1 = _decode(oracle_mod, wl, t, kc, cache_of(v1))
+    o2 = _decode(oracle_mod, wl, t, kc, cache_of(v2))
+    o12 = _decode(oracle_mod, wl, t, kc, cache_of(2 * v1 - 3 * v2))
+    assert np.abs(o1 - o2).max() > 0.1  # the two parts differ
+    np.testing.assert_allclose(o12, 2 * o1 - 3 * o2, rtol=0, atol=1e-12)
 
 
 def test_zero_length_gives_zeros(oracle_mod):
