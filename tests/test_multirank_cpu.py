@@ -63,3 +63,35 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     class Args:
         steps, warmup = 3, 3
     assert bench.run_reference(Args(), W.make_workload("tiny"), 4) is None
+
+
+def test_reference_arm_line_keeps_the_contract(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_gqa_06_gb300 import workloads as W
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+
+    class Args:
+        steps, warmup = 2, 1
+    line = bench.run_reference(Args(), W.make_workload("tiny"), 4)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["config"]["workload"].startswith("tiny")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_gqa_06_gb300 import workloads as W
+    cb = bench.cpu_baseline(W.make_workload("tiny"), 4, budget_s=0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0 and cb["cores"] >= 1
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "GB/s"
