@@ -99,11 +99,12 @@ struct PrefillParams {
 // Programmatic dependent launch.  The decode and append kernels are
 // launched with programmatic stream serialization: the next grid in the
 // stream may be launched once every CTA of this one has called
-// griddep_launch_dependents, and every kernel calls griddep_wait before its
-// first global memory access, which returns once the previous grid in the
-// stream has completed and its memory is visible.  Only the launch and CTA
-// start-up overlap; no data access does.  (Without the launch attribute both
-// are no-ops.)
+// griddep_launch_dependents, and every kernel calls griddep_wait, which
+// returns once the previous grid in the stream has completed and its memory
+// is visible, before any memory access whose value it uses and before any
+// write.  Only the launch, CTA start-up and (in the decode kernels) L2
+// prefetches of the first K/V tiles overlap.  (Without the launch attribute
+// both are no-ops.)
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -230,6 +231,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Prefetch one tiled box of a 4-D tensor map into L2: no shared memory, no
+// completion to track.  Coordinates outside the tensor fetch nothing; c0
+// times the element size must be a multiple of 16 bytes, as for a load.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 // Order this thread's generic-proxy shared-memory writes before later

@@ -23,8 +23,9 @@
 //     fill the n = 8 side).  Pass 1: logits S^T = K q^T, 16 tokens per tile,
 //     into shared memory in log2 units.  The split's max and sum are taken
 //     over all its logits at once (no running rescale).  Pass 2:
-//     O^T += V^T P^T with P split into bf16 high and low parts (two MMAs), so
-//     the weights keep ~16 bits of precision;
+//     O^T += V^T P^T with P split into bf16 high and low parts, so the
+//     weights keep ~16 bits of precision; for G <= 4 the low parts ride in
+//     the n columns no head uses, so this takes one MMA per 16 dims;
 //   * a split that is the whole sequence writes `out` directly.  Otherwise
 //     it writes unnormalised (acc, max, sum) to the workspace and counts
 //     itself in at a per-(b, g) arrival counter; the CTA that arrives last
@@ -36,8 +37,10 @@
 // a running maximum and sum instead of a logits buffer, so all of its shared
 // memory is K/V ring.  The host plan (abi.cu) gives splits of 512 tokens or
 // more to the single-pass kernel and shorter ones to the two-pass kernel.
-// Both are launched with programmatic stream serialization and touch no
-// global memory before griddepcontrol.wait.
+// Both are launched with programmatic stream serialization.  Before
+// griddepcontrol.wait a CTA only reads its sequence length and block-table
+// entries through L2 to prefetch its first K/V tiles into L2 (the values may
+// be stale and steer nothing else); everything it uses is read after the wait.
 // Slots at t >= L never reach the output: their logits are -inf and their V
 // rows are zeroed in shared memory before the PV product, so NaN in unused
 // slots cannot leak in.
@@ -55,6 +58,48 @@ constexpr int kStageBlocks = 2;              // KV blocks (tiles) per pipeline s
 constexpr int kConsumerWarps = kStageBlocks; // one tile per consumer warp per stage
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;    // + one producer warp
+
+// The n = 8 columns of the MMAs' B operands and accumulators (QK^T: the query
+// heads; P V: the softmax weights of those heads).  With G <= 4 heads per
+// group only columns 0-3 would carry heads, so column c holds head c % 4
+// (when that head exists): the same q in columns c and c + 4 gives the same
+// logits and weights there, and in P V columns 0-3 carry the weights' bf16
+// high part and columns 4-7 their low part.  One MMA per 16 dims then gives P
+// about 16 significant bits; the two halves of O are added once at the end.
+// At G = 8 every column is a head and P V takes two MMAs (high, then low).
+template <int G>
+struct PvCols {
+  static constexpr bool kPacked = G <= 4;
+  __device__ static __forceinline__ int head(int c) { return kPacked ? (c & 3) : c; }
+  __device__ static __forceinline__ bool valid(int c) { return head(c) < G; }
+  __device__ static __forceinline__ bool low(int c) { return kPacked && c >= 4; }
+};
+
+// B fragment of P^T for column `col` of a P V MMA from four weights: the
+// bf16 high parts, or for a packed low column the low parts (x - bf16(x)
+// rounded to bf16); `lo*` receive the low parts for the second MMA at G = 8.
+template <int G>
+__device__ __forceinline__ void p_fragment(int col, float2 pa, float2 pc, uint32_t& b0, uint32_t& b1, uint32_t& lo0,
+                                           uint32_t& lo1) {
+  split_bf16x2(pa.x, pa.y, b0, lo0);
+  split_bf16x2(pc.x, pc.y, b1, lo1);
+  if (PvCols<G>::low(col)) {
+    b0 = lo0;
+    b1 = lo1;
+  }
+}
+
+// Add each packed low column of the O^T accumulators into its high column
+// (lanes 4 apart in the accumulator layout: column 2 (lane % 4) + e).
+template <int G, int MT>
+__device__ __forceinline__ void fold_low_columns(float (&o)[MT][4]) {
+  if constexpr (PvCols<G>::kPacked) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+  }
+}
 
 struct SmemLayout {
   size_t ring, logits, red_ml, bars, total;
@@ -104,6 +149,92 @@ __device__ __forceinline__ int checked_length(const DecodeParams& p, int b, bool
     L = L < 0 ? 0 : Lmax;
   }
   return L;
+}
+
+// A load through L2 only (no L1 copy), for values read before the previous
+// grid in the stream has completed: they may be stale, and a later load of
+// the same address must not find them in L1.
+__device__ __forceinline__ int ld_cg(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
+// Split s of a sequence of L tokens.  Splits are aligned to the END of the
+// sequence: split nsplit-1 ends at its last block, every split but split 0
+// holds bps blocks and split 0 the remaining r = nblk - (nsplit-1) bps (1..bps).
+// The grid runs the highest split index first, so full splits are dispatched
+// before the partial ones and the tail of the last wave is made of short CTAs
+// (the longest-first order that evens out ragged batches).
+struct SplitWork {
+  int nblk, nsplit, blk0, n;
+};
+__device__ __forceinline__ SplitWork split_work(int L, int bps, int s) {
+  SplitWork w;
+  w.nblk = (L + kBlockSize - 1) / kBlockSize;
+  w.nsplit = (w.nblk + bps - 1) / bps;
+  const int r = w.nblk - (w.nsplit - 1) * bps;
+  w.blk0 = s == 0 ? 0 : r + (s - 1) * bps;
+  w.n = s == 0 ? r : bps;
+  return w;
+}
+
+// The block-table entries of split s, requested by the producer warp before
+// the length is known: for s >= 1 the split starts in [(s-1) bps + 1, s bps],
+// so the 2 bps - 1 entries from w0 = (s-1) bps + 1 (from 0 for s = 0) cover
+// it.  Lane l holds entries w0 + l + 32 k, k < 4 (bps <= 64); entries past
+// the row are 0 and never used.
+struct TableWindow {
+  int e0, e1, e2, e3, w0;
+  __device__ __forceinline__ void load(const DecodeParams& p, int b, int s, int lane) {
+    w0 = s == 0 ? 0 : (s - 1) * p.bps + 1;
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
+    const int end = min(p.MB, w0 + 2 * p.bps - 1);
+    const int i = w0 + lane;
+    e0 = i < end ? ld_nc_keep(row + i) : 0;
+    e1 = i + 32 < end ? ld_nc_keep(row + i + 32) : 0;
+    e2 = i + 64 < end ? ld_nc_keep(row + i + 64) : 0;
+    e3 = i + 96 < end ? ld_nc_keep(row + i + 96) : 0;
+  }
+  // the entry of block `blk` (warp-uniform) of the window, from its lane
+  __device__ __forceinline__ int entry(int blk) const {
+    const int i = blk - w0;
+    const int k = i >> 5;
+    return __shfl_sync(0xffffffffu, k == 0 ? e0 : k == 1 ? e1 : k == 2 ? e2 : e3, i & 31);
+  }
+  // any of the split's entries [blk0, blk0 + n) outside [0, NB)
+  __device__ __forceinline__ bool any_bad(int blk0, int n, int NB, int lane) const {
+    const int a = blk0 - w0, z = a + n;
+    const int i = lane;
+    const bool bad = (i >= a && i < z && static_cast<unsigned>(e0) >= static_cast<unsigned>(NB)) ||
+                     (i + 32 >= a && i + 32 < z && static_cast<unsigned>(e1) >= static_cast<unsigned>(NB)) ||
+                     (i + 64 >= a && i + 64 < z && static_cast<unsigned>(e2) >= static_cast<unsigned>(NB)) ||
+                     (i + 96 >= a && i + 96 < z && static_cast<unsigned>(e3) >= static_cast<unsigned>(NB));
+    return __any_sync(0xffffffffu, bad);
+  }
+};
+
+// Before griddepcontrol.wait: bring the K and V tiles of the first `stages`
+// ring stages of this CTA into L2 while the previous grid in the stream
+// finishes.  The length and table entries are read through L2 only and may
+// be stale: they steer prefetches alone (block ids are checked against the
+// pool, and the TMA engine bounds-checks tensor coordinates); every value
+// the kernel uses is read again after the wait.  One lane per block.
+template <int D>
+__device__ __forceinline__ void prefetch_first_stages(const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                                      const DecodeParams& p, int b, int g, int s, int stages,
+                                                      int lane) {
+  int L = ld_cg(p.context_lens + b);
+  L = L < 0 ? 0 : min(L, p.MB * kBlockSize);
+  const SplitWork w = split_work(L, p.bps, s);
+  if (s >= w.nsplit || lane >= min(w.n, stages * 2)) return;
+  const int pb = ld_cg(p.block_tables + static_cast<int64_t>(b) * p.bt_sb + w.blk0 + lane);
+  if (static_cast<unsigned>(pb) >= static_cast<unsigned>(p.NB)) return;
+#pragma unroll
+  for (int c = 0; c < D / kBoxDims; ++c) {
+    tma_prefetch_4d(tmk, c * kBoxDims, 0, g, pb);
+    tma_prefetch_4d(tmv, c * kBoxDims, 0, g, pb);
+  }
 }
 
 // Fused append: put this step's new row (`src`, D bf16) into row `r` of the
@@ -331,30 +462,26 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   constexpr int KSTEPS = D / 16;  // 16-dim MMA steps (QK) = 16-dim m-tiles (PV)
   static_assert(D % kBoxDims == 0 && G >= 1 && G <= 8, "shape not built");
 
-  // grid (KV head, sequence, split): all first splits are dispatched before
-  // any second split, so each sequence's shorter last split comes late.
-  const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
+  // grid (KV head, sequence, split slot): the highest split index runs
+  // first (split_work: splits are aligned to the end of the sequence).
+  const int g = blockIdx.x, b = blockIdx.y, s = static_cast<int>(gridDim.z - 1 - blockIdx.z);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
-  griddep_wait();  // no global access before the previous grid in the stream is complete
+  if (warp == kConsumerWarps) prefetch_first_stages<D>(&tmk, &tmv, p, b, g, s, p.nstage, lane);
+  griddep_wait();  // every value used below is read after the previous grid in the stream is complete
 
   // The producer's block-table entries for this split are requested with the
-  // length, not after it (entries past the sequence are loaded but unused;
-  // the row has MB entries).
-  int e0 = 0, e1 = 0;
+  // length, not after it (a window that covers the split wherever the length
+  // puts it; entries past the sequence are loaded but unused).
+  TableWindow tw;
   if (warp == kConsumerWarps) {
     if (lane == 0) {  // the TMA descriptors, fetched while the length and table are read
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
-    const int room = min(p.bps, p.MB - s * p.bps);
-    if (lane < room) e0 = ld_nc_keep(row + lane);
-    if (lane + 32 < room) e1 = ld_nc_keep(row + 32 + lane);
+    tw.load(p, b, s, lane);
   }
   const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
-  const int nblk = (L + kBlockSize - 1) / kBlockSize;
-  const int nsplit = (nblk + p.bps - 1) / p.bps;
 
   if (L == 0) {  // empty context: the output is defined as zero
     if (s == 0) {
@@ -365,22 +492,11 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
     }
     return;
   }
+  const SplitWork sw = split_work(L, p.bps, s);
+  const int nsplit = sw.nsplit;
   if (s >= nsplit) return;
-
-  // A sequence of two splits gets two halves instead of a full split and a
-  // short tail (1100 tokens: 2 x 35 blocks, not 64 + 5), which evens out the
-  // CTAs of batches with many such sequences.  Longer sequences keep full
-  // splits: evening all of them out made equal CTAs that spill into a small
-  // extra wave (uniform 4352-token batch: 102.7 against 90.6 us).  Either way
-  // the split starts inside the sequence (blk0 <= (nsplit - 1) * bps < nblk).
-  const int bpsb = nsplit == 2 ? (nblk + 1) / 2 : p.bps;
-  const int blk0 = s * bpsb;
-  const int n = min(bpsb, nblk - blk0);                   // KV blocks in this split (>= 1)
-  if (warp == kConsumerWarps && blk0 != s * p.bps) {      // the entries requested early were for s * bps
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0;
-    e0 = lane < n ? __ldg(row + lane) : 0;
-    e1 = lane + 32 < n ? __ldg(row + 32 + lane) : 0;
-  }
+  const int blk0 = sw.blk0;
+  const int n = sw.n;  // KV blocks in this split (>= 1)
   const int nks = (n + kStageBlocks - 1) / kStageBlocks;  // stages per pass
   const int nstage = p.nstage;
 
@@ -408,9 +524,7 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
-                     (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
+    if (tw.any_bad(blk0, n, p.NB, lane) && lane == 0) record_error(p.err, kDevErrBlockId);
     int slot = 0;
     uint32_t phase = 0;
     for (int i = 0; i < 2 * nks; ++i) {
@@ -419,9 +533,8 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
       int pb[kStageBlocks];
 #pragma unroll
       for (int u = 0; u < kStageBlocks; ++u) {
-        const int j = j0 + u;  // <= 64
-        pb[u] = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
-        if (j >= n) pb[u] = -1;  // past the split: no tile
+        const int j = j0 + u;  // < bps + 1
+        pb[u] = j < n ? tw.entry(blk0 + j) : -1;  // past the split: no tile
       }
       if (lane == 0) {
         if (i >= nstage) mbar_wait(empty + slot, phase ^ 1u, p.err);  // stage released
@@ -464,13 +577,15 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
   const bool qk_path = p.q_norm_w != nullptr || p.k_norm_w != nullptr || p.rope != nullptr;
   const bool rope = p.rope != nullptr && pos < p.rope_rows;
   if (p.rope != nullptr && !rope && tid == 0 && s == 0 && g == 0) record_error(p.err, kDevErrPosition);
+  const bool col_ok = PvCols<G>::valid(tq);  // column tq of the B operands holds a head
   uint32_t qb[KSTEPS][2];
   {
-    const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + tq) * p.q_sh;
+    const __nv_bfloat16* qrow =
+        p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + PvCols<G>::head(tq)) * p.q_sh;
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
-      qb[ks][0] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
-      qb[ks][1] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
+      qb[ks][0] = col_ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
+      qb[ks][1] = col_ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
     }
     if (qk_path) {  // uniform across the CTA
       float x[KSTEPS][4];
@@ -484,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
       q_norm_rope<D>(x, tr, p, pos, rope);
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
-        qb[ks][0] = tq < G ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
-        qb[ks][1] = tq < G ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
+        qb[ks][0] = col_ok ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
+        qb[ks][1] = col_ok ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
       }
     }
   }
@@ -617,14 +732,13 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
       if (fused && j == jl)
         patch_new_row<D>(ring + (slot * kStageBlocks + warp) * TILE_BYTES,
                          p.v_new + static_cast<int64_t>(b) * p.vn_sb + g * p.vn_sh, vdst, rl, lane);
-      // B operand P^T (k = token, n = head): {p[tq][2tr], +1}, {p[tq][8 + 2tr], +1}
+      // B operand P^T (k = token, n = column tq): {p[2tr], +1}, {p[8 + 2tr], +1}
+      // of the column's head, high or low part (PvCols)
       uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
-      if (tq < G) {
-        const float* pr = logits + tq * lrow + j * kBlockSize + 2 * tr;
-        const float2 pa = *reinterpret_cast<const float2*>(pr);
-        const float2 pc = *reinterpret_cast<const float2*>(pr + 8);
-        split_bf16x2(pa.x, pa.y, bh0, bl0);
-        split_bf16x2(pc.x, pc.y, bh1, bl1);
+      if (col_ok) {
+        const float* pr = logits + PvCols<G>::head(tq) * lrow + j * kBlockSize + 2 * tr;
+        p_fragment<G>(tq, *reinterpret_cast<const float2*>(pr), *reinterpret_cast<const float2*>(pr + 8), bh0, bh1,
+                      bl0, bl1);
       }
       const int arow = (lane & 7) + (lane >> 4) * 8;  // token row this lane addresses
       const int acol = (lane >> 3) & 1;               // +0 / +1 chunk
@@ -633,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
         uint32_t a[4];
         ldsm_x4_trans(swz(tile, arow, 2 * mt + acol), a);
         mma_16816_bf16(o[mt], a, bh0, bh1);
-        mma_16816_bf16(o[mt], a, bl0, bl1);
+        if (!PvCols<G>::kPacked) mma_16816_bf16(o[mt], a, bl0, bl1);
       }
     }
     __syncwarp();
@@ -646,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
 
   // ---- merge the consumer warps' partial O through shared memory (the ring
   // is free: every stage has been consumed)
+  fold_low_columns<G>(o);
   named_barrier(1, kConsumers);
   {
     const int h0 = 2 * tr, h1 = 2 * tr + 1;
@@ -768,31 +883,28 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   constexpr int TILE_BYTES = kBlockSize * D * 2;
   constexpr int BOXES = D / kBoxDims;
   constexpr int KSTEPS = D / 16;
-  constexpr bool kPLow = !std::is_same<OutT, __nv_bfloat16>::value;  // P's low part in P V
   static_assert(D % kBoxDims == 0 && G >= 1 && G <= 8, "shape not built");
 
-  const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
+  // grid (KV head, sequence, split slot): the highest split index runs
+  // first (split_work: splits are aligned to the end of the sequence).
+  const int g = blockIdx.x, b = blockIdx.y, s = static_cast<int>(gridDim.z - 1 - blockIdx.z);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
-  griddep_wait();  // no global access before the previous grid in the stream is complete
+  if (warp == kConsumerWarps) prefetch_first_stages<D>(&tmk, &tmv, p, b, g, s, p.nstage, lane);
+  griddep_wait();  // every value used below is read after the previous grid in the stream is complete
 
   // The producer's block-table entries for this split are requested with the
-  // length, not after it (entries past the sequence are loaded but unused;
-  // the row has MB entries).
-  int e0 = 0, e1 = 0;
+  // length, not after it (a window that covers the split wherever the length
+  // puts it; entries past the sequence are loaded but unused).
+  TableWindow tw;
   if (warp == kConsumerWarps) {
     if (lane == 0) {  // the TMA descriptors, fetched while the length and table are read
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + s * p.bps;
-    const int room = min(p.bps, p.MB - s * p.bps);
-    if (lane < room) e0 = ld_nc_keep(row + lane);
-    if (lane + 32 < room) e1 = ld_nc_keep(row + 32 + lane);
+    tw.load(p, b, s, lane);
   }
   const int L = checked_length(p, b, s == 0 && g == 0 && threadIdx.x == 0);
-  const int nblk = (L + kBlockSize - 1) / kBlockSize;
-  const int nsplit = (nblk + p.bps - 1) / p.bps;
 
   if (L == 0) {  // empty context: the output is defined as zero
     if (s == 0) {
@@ -803,22 +915,11 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
     }
     return;
   }
+  const SplitWork sw = split_work(L, p.bps, s);
+  const int nsplit = sw.nsplit;
   if (s >= nsplit) return;
-
-  // A sequence of two splits gets two halves instead of a full split and a
-  // short tail (1100 tokens: 2 x 35 blocks, not 64 + 5), which evens out the
-  // CTAs of batches with many such sequences.  Longer sequences keep full
-  // splits: evening all of them out made equal CTAs that spill into a small
-  // extra wave (uniform 4352-token batch: 102.7 against 90.6 us).  Either way
-  // the split starts inside the sequence (blk0 <= (nsplit - 1) * bps < nblk).
-  const int bpsb = nsplit == 2 ? (nblk + 1) / 2 : p.bps;
-  const int blk0 = s * bpsb;
-  const int n = min(bpsb, nblk - blk0);                   // KV blocks in this split (>= 1)
-  if (warp == kConsumerWarps && blk0 != s * p.bps) {      // the entries requested early were for s * bps
-    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb + blk0;
-    e0 = lane < n ? __ldg(row + lane) : 0;
-    e1 = lane + 32 < n ? __ldg(row + 32 + lane) : 0;
-  }
+  const int blk0 = sw.blk0;
+  const int n = sw.n;  // KV blocks in this split (>= 1)
   const int nst = (n + kStageBlocks - 1) / kStageBlocks;  // stages (K and V of 2 blocks each)
   const int nstage = p.nstage;
 
@@ -845,18 +946,15 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const bool bad = (lane < n && static_cast<unsigned>(e0) >= static_cast<unsigned>(p.NB)) ||
-                     (lane + 32 < n && static_cast<unsigned>(e1) >= static_cast<unsigned>(p.NB));
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(p.err, kDevErrBlockId);
+    if (tw.any_bad(blk0, n, p.NB, lane) && lane == 0) record_error(p.err, kDevErrBlockId);
     int slot = 0;
     uint32_t phase = 0;
     for (int st = 0; st < nst; ++st) {
       int pb[kStageBlocks];
 #pragma unroll
       for (int u = 0; u < kStageBlocks; ++u) {
-        const int j = st * kStageBlocks + u;  // <= 64
-        pb[u] = __shfl_sync(0xffffffffu, j < 32 ? e0 : e1, j & 31);
-        if (j >= n) pb[u] = -1;  // past the split: no tile
+        const int j = st * kStageBlocks + u;  // < bps + 1
+        pb[u] = j < n ? tw.entry(blk0 + j) : -1;  // past the split: no tile
       }
       if (lane == 0) {
         if (st >= nstage) mbar_wait(empty + slot, phase ^ 1u, p.err);  // stage released
@@ -902,13 +1000,15 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
   const bool qk_path = p.q_norm_w != nullptr || p.k_norm_w != nullptr || p.rope != nullptr;
   const bool rope = p.rope != nullptr && pos < p.rope_rows;
   if (p.rope != nullptr && !rope && tid == 0 && s == 0 && g == 0) record_error(p.err, kDevErrPosition);
+  const bool col_ok = PvCols<G>::valid(tq);  // column tq of the B operands holds a head
   uint32_t qb[KSTEPS][2];
   {
-    const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + tq) * p.q_sh;
+    const __nv_bfloat16* qrow =
+        p.q + static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(g * G + PvCols<G>::head(tq)) * p.q_sh;
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
-      qb[ks][0] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
-      qb[ks][1] = tq < G ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
+      qb[ks][0] = col_ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tr)) : 0u;
+      qb[ks][1] = col_ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tr)) : 0u;
     }
     if (qk_path) {  // uniform across the CTA
       float x[KSTEPS][4];
@@ -922,8 +1022,8 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
       q_norm_rope<D>(x, tr, p, pos, rope);
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
-        qb[ks][0] = tq < G ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
-        qb[ks][1] = tq < G ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
+        qb[ks][0] = col_ok ? pack_bf16x2(x[ks][0], x[ks][1]) : 0u;
+        qb[ks][1] = col_ok ? pack_bf16x2(x[ks][2], x[ks][3]) : 0u;
       }
     }
   }
@@ -1033,22 +1133,15 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
       __syncwarp();
       if (fused && j == jl)
         patch_new_row<D>(vt, p.v_new + static_cast<int64_t>(b) * p.vn_sb + g * p.vn_sh, vdst, rl, lane);
-      // ---- O^T += V^T P^T.  For fp32 output P goes in as bf16 high + low
-      // parts (~16 significant bits); for bf16 output it is rounded to bf16
-      // once (relative error 2^-9, no more than the output's own rounding),
-      // which halves the MMAs of this product.
+      // ---- O^T += V^T P^T, P as bf16 high + low parts (~16 significant
+      // bits, whatever the output type): for G <= 4 in one MMA per 16 dims,
+      // the low parts in the columns no head uses (PvCols), else two MMAs.
+      // Column tq of the scratch holds the weights of its head (columns c
+      // and c + 4 are equal when packed).
       uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
-      if (tq < G) {
-        const float2 pa = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 2 * tr);
-        const float2 pc = *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 8 + 2 * tr);
-        if (kPLow) {
-          split_bf16x2(pa.x, pa.y, bh0, bl0);
-          split_bf16x2(pc.x, pc.y, bh1, bl1);
-        } else {
-          bh0 = pack_bf16x2(pa.x, pa.y);
-          bh1 = pack_bf16x2(pc.x, pc.y);
-        }
-      }
+      if (col_ok)
+        p_fragment<G>(tq, *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 2 * tr),
+                      *reinterpret_cast<const float2*>(psc + tq * kBlockSize + 8 + 2 * tr), bh0, bh1, bl0, bl1);
       {
         const int arow = (lane & 7) + (lane >> 4) * 8;  // token row this lane addresses
         const int acol = (lane >> 3) & 1;               // +0 / +1 chunk
@@ -1057,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
           uint32_t a[4];
           ldsm_x4_trans(swz(vt_s, arow, 2 * mt + acol), a);
           mma_16816_bf16(o[mt], a, bh0, bh1);
-          if (kPLow) mma_16816_bf16(o[mt], a, bl0, bl1);
+          if (!PvCols<G>::kPacked) mma_16816_bf16(o[mt], a, bl0, bl1);
         }
       }
     }
@@ -1072,6 +1165,7 @@ __global__ void __launch_bounds__(kThreads) paged_gqa_decode_online_kernel(const
 
   // ---- merge the two warps' states: per head, the common maximum M; each
   // warp's O and sum scaled by 2^(m_w - M) (0 for a warp that had no block)
+  fold_low_columns<G>(o);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);

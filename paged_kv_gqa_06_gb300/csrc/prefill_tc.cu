@@ -22,11 +22,11 @@
 //     maximum grows by more than 8 in log2 units, so the weights stay <= 2^8
 //     and O in TMEM is rescaled rarely.  The weights P = 2^(scale s - m) are
 //     stored over the row's S in TMEM, two per column in its first 32
-//     columns.  For fp32 output they are split into bf16 high and low parts
-//     (low in the next 32 columns; two MMAs keep ~16 bits of each weight, as
-//     in the decode); for bf16 output they are rounded to bf16 once (relative
-//     error 2^-9, below the output's own rounding) and P V takes one MMA per K
-//     step.  At the end O is divided by the row sum and stored;
+//     columns, as bf16 high and low parts (low in the next 32 columns; two
+//     MMAs keep ~16 bits of each weight, as in the decode).  A weight rounded
+//     to bf16 once would lose up to 2^-8 of itself, which at |V| near 8 is as
+//     large as a bf16 output's own rounding.  At the end O is divided by the
+//     row sum and stored;
 //   * warp 5 (MMA) owns 256 TMEM columns: S (64), Q (D / 2: two bf16 per
 //     column) and the output accumulator O (D).  Its lane 0 issues
 //     S_j = Q K_j^T (M 128, N 64, K = D; Q from TMEM, K K-major straight from
@@ -44,7 +44,6 @@
 // but 0 * NaN is NaN.  Every mbarrier wait is bounded; the MMA warp drains
 // its own MMAs before TMEM is freed.
 #include <atomic>
-#include <type_traits>
 
 #include "common.cuh"
 #include "tcgen05.cuh"
@@ -153,9 +152,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   constexpr int QT = kTcRows / G;            // query tokens per CTA
-  // P as bf16 high + low parts (two P V MMAs) for fp32 output; one rounded
-  // bf16 part for bf16 output, whose own rounding is coarser than that of P
-  constexpr bool kPLow = !std::is_same<OutT, __nv_bfloat16>::value;
   constexpr int BOXES = D / 64;
   constexpr int KSTEPS = D / 16;
   constexpr TcLayout lay = tc_layout(D);
@@ -307,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int kk = 0; kk < kTcKv / 16; ++kk) {
               const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
               tc::mma_bf16_ts(tmem + kColO, phi + 8 * kk, bd, IDESC_O, jp > 0 || kk > 0);
-              if (kPLow) tc::mma_bf16_ts(tmem + kColO, plo + 8 * kk, bd, IDESC_O, true);
+              tc::mma_bf16_ts(tmem + kColO, plo + 8 * kk, bd, IDESC_O, true);
             }
             tc::commit(smem_addr(bars + kPvDone));
             tc::commit(smem_addr(bars + kKvEmpty + stp));
@@ -411,9 +407,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tc::wait_st();
       }
       // P = 2^(scale s - m_used) <= 2^8 over S in TMEM, two weights per
-      // column in columns [0, 32) of the buffer; for fp32 output as bf16 high
-      // and low parts (low in [32, 64)), for bf16 output rounded to bf16 once;
-      // in two halves of 32 weights
+      // column in columns [0, 32) of the buffer as bf16 high parts and the
+      // low parts in [32, 64); in two halves of 32 weights
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t hi[16], lo[16];
@@ -422,13 +417,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const float a = fast_exp2(fmaf(s[32 * h + 2 * e], scale, -m_used));
           const float c = fast_exp2(fmaf(s[32 * h + 2 * e + 1], scale, -m_used));
           l += a + c;
-          if (kPLow)
-            split_bf16x2(a, c, hi[e], lo[e]);
-          else
-            hi[e] = pack_bf16x2(a, c);
+          split_bf16x2(a, c, hi[e], lo[e]);
         }
         tc::st_32x32b_x16(trow + kColS + 16 * h, hi);
-        if (kPLow) tc::st_32x32b_x16(trow + kColS + kTcKv / 2 + 16 * h, lo);
+        tc::st_32x32b_x16(trow + kColS + kTcKv / 2 + 16 * h, lo);
       }
       tc::wait_st();
       if (j == nkv - 1) {

@@ -23,6 +23,8 @@ Recipe (every config):
     4 Mi-element chunk, seeded by (seed, layer, tensor, chunk)), rounded to
     bf16 with round-to-nearest-even.  Config "qwen3_4b" doubles K (an exact power-of-two
     scale) so that logits reach about +-8.
+  * Values "rounding_stress" (tests only): structured q/K/V for the worst
+    case of the output precision -- see rounding_stress_values.
   * Poison: every cache slot that holds no token before the append -- free
     blocks, the tail of each sequence's last block, and the append target
     itself -- is bf16 NaN (0x7FC0), so a kernel that reads a slot it should
@@ -113,6 +115,7 @@ class Spec:
     layers: int = 1
     seed: int = 0
     chunk: int = 0            # prefill: new tokens per sequence (0 = the whole context)
+    values: str = "normal"    # "normal" or "rounding_stress" (see rounding_stress_values)
     description: str = ""
 
 
@@ -155,6 +158,41 @@ SPECS = {
 }
 
 
+# Logit gap of the rounding-stress values: exp(-7.8125 / sqrt(128)) = 0.50131,
+# just above 0.5, so a softmax weight rounded to bf16 (steps of 2^-8 there)
+# loses 0.26 % of itself.  7.8125 is exact in bf16.
+STRESS_GAP = 7.8125
+
+
+def rounding_stress_values(spec: Spec, key, rows: int, slot_of_row, nb: int):
+    """q [rows, Hq, D], k/v of the new rows [rows, Hkv, D] and caches [nb, Hkv, 16, D]
+    (bf16 bits) for the worst case of the output precision: every softmax
+    weight but one per block sits just above 0.5, where rounding it to bf16
+    drops about 2^-8.6 of it in the same direction, and every V value is
+    large (magnitude in [7, 8), one sign per (KV head, dim)), so the output
+    is too.  Query head h has a single 1 at dim h % G; key dims < G hold
+    STRESS_GAP in slot 0 of every block and 0 elsewhere, so slot 0 of each
+    block is the maximum and the other 15 tokens get weight exp(-gap scale).
+    ``slot_of_row(r)`` is the cache slot (0..15) of new row r."""
+    G, D = spec.Hq // spec.Hkv, spec.D
+    rng = np.random.default_rng([*key, 0x5735])
+    q = np.zeros((rows, spec.Hq, D), dtype=np.float32)
+    for h in range(spec.Hq):
+        q[:, h, h % G] = 1.0
+    kc = rng.standard_normal((nb, spec.Hkv, BLOCK_SIZE, D), dtype=np.float32)
+    kc[:, :, :, :G] = 0.0
+    kc[:, :, 0, :G] = STRESS_GAP
+    kn = rng.standard_normal((rows, spec.Hkv, D), dtype=np.float32)
+    kn[:, :, :G] = 0.0
+    for r in range(rows):
+        if slot_of_row(r) == 0:
+            kn[r, :, :G] = STRESS_GAP
+    sign = np.where(rng.random((spec.Hkv, D)) < 0.5, -1.0, 1.0).astype(np.float32)
+    vc = sign[None, :, None, :] * rng.uniform(7.0, 7.97, (nb, spec.Hkv, BLOCK_SIZE, D)).astype(np.float32)
+    vn = sign[None, :, :] * rng.uniform(7.0, 7.97, (rows, spec.Hkv, D)).astype(np.float32)
+    return tuple(f32_to_bf16_bits(x) for x in (q, kn, vn, kc, vc))
+
+
 @dataclasses.dataclass
 class Workload:
     """One batch of decode inputs.  Arrays are numpy; bf16 tensors are uint16 bits.
@@ -193,12 +231,16 @@ class Workload:
         """q, k_new, v_new and the pre-append (poisoned) caches of layer ``l``."""
         s = self.spec
         key = (self.seed, 1 + l)
-        q = _normal_bf16((*key, 0), (s.B, s.Hq, s.D))
-        k_new = _normal_bf16((*key, 1), (s.B, s.Hkv, s.D), s.k_mul)
-        v_new = _normal_bf16((*key, 2), (s.B, s.Hkv, s.D))
-        shape = (self.NB, s.Hkv, BLOCK_SIZE, s.D)
-        k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
-        v_cache = _normal_bf16((*key, 4), shape)
+        if s.values == "rounding_stress":
+            q, k_new, v_new, k_cache, v_cache = rounding_stress_values(
+                s, key, s.B, lambda b: (int(self.context_lens[b]) - 1) % BLOCK_SIZE, self.NB)
+        else:
+            q = _normal_bf16((*key, 0), (s.B, s.Hq, s.D))
+            k_new = _normal_bf16((*key, 1), (s.B, s.Hkv, s.D), s.k_mul)
+            v_new = _normal_bf16((*key, 2), (s.B, s.Hkv, s.D))
+            shape = (self.NB, s.Hkv, BLOCK_SIZE, s.D)
+            k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
+            v_cache = _normal_bf16((*key, 4), shape)
         pb, po = np.nonzero(self.poison_mask())
         k_cache[pb, :, po, :] = BF16_NAN
         v_cache[pb, :, po, :] = BF16_NAN
@@ -350,12 +392,16 @@ class PrefillWorkload:
         """q [T,Hq,D], the chunk's k/v [T,Hkv,D] and the pre-append caches of layer ``l``."""
         s = self.base.spec
         key = (self.base.seed, 1 + l)
-        q = _normal_bf16((*key, 10), (self.T, s.Hq, s.D))
-        k_new = _normal_bf16((*key, 11), (self.T, s.Hkv, s.D), s.k_mul)
-        v_new = _normal_bf16((*key, 12), (self.T, s.Hkv, s.D))
-        shape = (self.base.NB, s.Hkv, BLOCK_SIZE, s.D)
-        k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
-        v_cache = _normal_bf16((*key, 4), shape)
+        if s.values == "rounding_stress":
+            q, k_new, v_new, k_cache, v_cache = rounding_stress_values(
+                s, key, self.T, lambda r: int(self.slot_mapping[r]) % BLOCK_SIZE, self.base.NB)
+        else:
+            q = _normal_bf16((*key, 10), (self.T, s.Hq, s.D))
+            k_new = _normal_bf16((*key, 11), (self.T, s.Hkv, s.D), s.k_mul)
+            v_new = _normal_bf16((*key, 12), (self.T, s.Hkv, s.D))
+            shape = (self.base.NB, s.Hkv, BLOCK_SIZE, s.D)
+            k_cache = _normal_bf16((*key, 3), shape, s.k_mul)
+            v_cache = _normal_bf16((*key, 4), shape)
         pb, po = np.nonzero(self.base.poison_mask(self.chunk_lens))
         k_cache[pb, :, po, :] = BF16_NAN
         v_cache[pb, :, po, :] = BF16_NAN

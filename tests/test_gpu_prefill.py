@@ -6,8 +6,8 @@ token; bit-exact against the oracle's append), then runs the prefill and
 compares every output row with oracle.paged_prefill within the parity
 tolerance.  Covers every instantiation (D 64 / 128, G 1 / 2 / 4 / 8, fp32 /
 bf16 out), runs that are whole prompts, single tokens, empty, or cross block
-and stage boundaries, the Qwen3-4B-shaped batch at full size (sampled
-sequences), graph capture, and the device-side check of query_start.
+and stage boundaries, the Qwen3-4B-shaped batch at full size (every
+sequence), graph capture, and the device-side check of query_start.
 """
 import numpy as np
 import pytest
@@ -118,7 +118,7 @@ def test_one_token_runs_match_the_decode():
     assert max_abs_err(pre, ref) <= TOL["f32"] and max_abs_err(dec, ref) <= TOL["f32"]
 
 
-def test_prefill_qwen3_4b_full_size_sampled():
+def test_prefill_qwen3_4b_full_size():
     pw = W.make_prefill("prefill_4b")
     t = pw.layer(0)
     d = DevicePrefill(pw, t)
@@ -130,11 +130,11 @@ def test_prefill_qwen3_4b_full_size_sampled():
     kc_ref, vc_ref = t["k_cache"].copy(), t["v_cache"].copy()
     oracle.paged_kv_append(t["k_new"], t["v_new"], pw.slot_mapping, kc_ref, vc_ref)
     assert np.array_equal(kc, kc_ref) and np.array_equal(vc, vc_ref)
-    for b in (0, 3, 7):                                    # sampled sequences, all their query rows
+    ref = oracle.paged_prefill(t["q"], kc_ref, vc_ref, pw.block_tables, pw.context_lens, pw.query_start,
+                               pw.scale)                  # every sequence, every query row
+    for b in range(pw.B):
         q0, q1 = int(pw.query_start[b]), int(pw.query_start[b + 1])
-        ref = oracle.paged_prefill(t["q"][q0:q1], kc_ref, vc_ref, pw.block_tables[b:b + 1],
-                                   pw.context_lens[b:b + 1], np.array([0, q1 - q0], np.int32), pw.scale)
-        assert max_abs_err(out[q0:q1], ref) <= TOL["bf16"], b
+        assert max_abs_err(out[q0:q1], ref[q0:q1]) <= TOL["bf16"], b
 
 
 def test_prefill_graph_capture():
@@ -172,4 +172,22 @@ def test_empty_batch_is_a_no_op():
     d = DevicePrefill(pw, pw.layer(0))
     out = torch.empty(0, pw.Hq, pw.D, dtype=torch.float32, device=DEV)
     binding.forge_paged_prefill(d.q, d.k_cache, d.v_cache, d.tables, d.lens, d.qs, pw.scale, out)
+    assert binding.forge_paged_get_device_error() == 0
+
+
+def test_prefill_rounding_stress():
+    """The worst case of the output precision (workloads.rounding_stress_values):
+    weights just above 0.5 and |V| in [7, 8); see tests/test_gpu_precision.py."""
+    spec = W.custom_spec("pf_stress", B=3, Hq=32, Hkv=8, D=128, fixed_lens=(1500, 700, 129), free_frac=0.1,
+                         seed=413, values="rounding_stress")
+    pw = W.make_prefill(spec, chunk_lens=(512, 700, 64))
+    t = pw.layer(0)
+    _, _, ref = _oracle(pw, t)
+    assert np.abs(ref).min() >= 7.0
+    d = DevicePrefill(pw, t)
+    d.append()
+    for od in ("f32", "bf16"):
+        err = max_abs_err(d.prefill(od), ref)
+        print(f"prefill rounding stress out={od}: max-abs error {err:.3e}")
+        assert err <= TOL[od], f"{od}: {err}"
     assert binding.forge_paged_get_device_error() == 0
