@@ -30,8 +30,10 @@
  * can be captured in a CUDA graph (see forge_paged_gqa_decode for its
  * workspace note).  The append and decode kernels are launched with
  * programmatic stream serialization, so their start-up may overlap the end of
- * the previous kernel in the stream, but none touches memory before that
- * kernel has completed: stream order holds as for a plain launch.  Calls
+ * the previous kernel in the stream.  Before that kernel has completed, a
+ * decode kernel only reads its sequence lengths and block-table entries to
+ * prefetch its first K/V tiles into L2; it writes nothing and uses no value
+ * read then, so stream order holds as for a plain launch.  Calls
  * never abort, throw or trap: they return a forge_status.  Argument errors are reported before anything is enqueued.
  * Violations of the device-side preconditions (a block id outside the pool,
  * a length longer than the table row, a slot outside the pool) make the
@@ -148,19 +150,22 @@ FORGE_API int forge_paged_kv_append(const forge_tensor *k_new, const forge_tenso
  * Arithmetic: products of bf16 values on the tensor cores with fp32
  * accumulation; softmax, sums and the split merge in fp32.  The softmax
  * weights enter the P V product as bf16 high + low parts (about 16
- * significant bits) for f32 output; with bf16 output the single-pass kernel
- * rounds them to bf16 once (relative error 2^-9).  The parity tests hold the
- * result within 2e-3 (f32 out) or 1.6e-2 (bf16 out) max-abs of exact
- * attention, for values of the size of N(0, 1) inputs (|V| < 8).  The split scratch is a per-(device, stream) buffer
- * that the library allocates with cudaMalloc (and zero-fills) on first need
- * and keeps, growing it when a larger problem arrives; the first call of a
- * given size on a stream should therefore come before any stream capture.
- * Use forge_paged_gqa_decode_ex to pass caller-owned scratch instead.
- * Thread-safe for calls on different streams.  Calls from several host
- * threads on ONE stream must be ordered by the caller: growing that stream's
- * scratch frees the old buffer once the stream's queued work is done, and a
- * call that fetched the old buffer but had not yet enqueued its kernel would
- * then use freed memory.
+ * significant bits) whatever the output type, so the error of the result
+ * before its final rounding stays near 1e-5 of max|V|.  The parity tests
+ * hold the result within 2e-3 (f32 out) or 1.6e-2 (bf16 out) max-abs of
+ * exact attention, including a case built to make rounded weights fail
+ * (outputs near 7.5, where bf16's own rounding is up to 2^-6).
+ * Split scratch: a per-(device, stream) buffer that the library owns.  It is
+ * allocated on first need and grown when a larger problem arrives, in stream
+ * order on `stream` (cudaMallocAsync, zero-filled by cudaMemsetAsync; the old
+ * buffer goes back with cudaFreeAsync after the work queued before it), so no
+ * call synchronises the host.  While `stream` is being captured into a CUDA
+ * graph the scratch cannot grow: such a call returns FORGE_ERR_WORKSPACE
+ * before enqueuing anything, so make the first call of the largest size on a
+ * stream before capturing it.  Use forge_paged_gqa_decode_ex to pass
+ * caller-owned scratch instead.  Thread-safe, also for several host threads
+ * on one stream: a call holds its stream's scratch from lookup until its
+ * kernel is enqueued.
  */
 FORGE_API int forge_paged_gqa_decode(const forge_tensor *q, const forge_tensor *k_cache,
                            const forge_tensor *v_cache, const forge_tensor *block_tables,
@@ -231,8 +236,8 @@ FORGE_API int forge_paged_gqa_decode_ex(const forge_tensor *q, const forge_tenso
  * A sequence with L_b = 0 appends nothing.  The kernel that reads the
  * sequence's last block writes the new row into it (in shared memory and in
  * the cache), so no other launch is needed; the block holding position
- * L_b - 1 must not be read by another sequence of the same call.  Scratch as
- * in forge_paged_gqa_decode (library-owned).
+ * L_b - 1 must not be read by another sequence of the same call.  Scratch,
+ * its growth and thread-safety as in forge_paged_gqa_decode (library-owned).
  */
 FORGE_API int forge_paged_append_gqa_decode(const forge_tensor *q, const forge_tensor *k_new,
                                   const forge_tensor *v_new, forge_tensor *k_cache,
@@ -292,13 +297,14 @@ FORGE_API int forge_rope_cos_sin_table(double theta, int D, int rows, float *out
  * must not allocate device memory.  (The pages have no counterpart: this is
  * an entry point of this library only.)
  *
- * Who needs it: code that decodes while a stream is being captured into a
- * CUDA graph, where cudaMalloc (not a stream operation, and synchronising) is
- * not allowed, and processes that fix their device memory at start-up -- a
- * serving loop that gave everything else to its KV pool -- and must not
- * allocate later.  forge_paged_gqa_decode may cudaMalloc its split scratch on
- * first use; this call never calls cudaMalloc, cudaFree or any allocating
- * routine.
+ * Who needs it: processes that fix their device memory at start-up and
+ * must not allocate later -- a serving loop that handed everything left over
+ * to its KV-block pool, where a later allocation fails or evicts cache
+ * blocks -- and callers that run under a memory manager of their own (an
+ * embedding runtime or framework allocator) that forbids allocations it did
+ * not make.  forge_paged_gqa_decode may allocate its split scratch on first
+ * use; this call never calls cudaMalloc, cudaMallocAsync, cudaFree or any
+ * other allocating routine.
  *
  * Arguments, layouts, results and errors are those of forge_paged_gqa_decode.
  * The split scratch is a static device array of FORGE_NOALLOC_SCRATCH_BYTES
@@ -325,7 +331,6 @@ FORGE_API int forge_paged_gqa_decode_noalloc(const forge_tensor *q, const forge_
                                    const forge_tensor *context_lens, float scale, forge_tensor *out,
                                    void *stream);
 
-/* Human-readable name of a forge_status.  Never NULL. */
 /*
  * forge_paged_prefill -- causal attention of a run of new query tokens per
  * sequence over its paged cache ("Make the Engine Talk", 1.2: the prefill
@@ -361,6 +366,7 @@ FORGE_API int forge_paged_prefill(const forge_tensor *q, const forge_tensor *k_c
                                   const forge_tensor *context_lens, const forge_tensor *query_start,
                                   float scale, forge_tensor *out, void *stream);
 
+/* Human-readable name of a forge_status.  Never NULL. */
 FORGE_API const char *forge_status_string(int status);
 
 /*

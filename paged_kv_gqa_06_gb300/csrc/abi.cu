@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <utility>
 
@@ -33,8 +34,17 @@ constexpr int kMinSplitTokens = 16;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
-// Split workspace owned by the library, per (device, stream).
-std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_workspaces;
+
+// Split workspace owned by the library, one per (device, stream).  Its own
+// mutex is held from the lookup until the kernel that uses it is enqueued, so
+// a call that grows it (and releases the old buffer in stream order) never
+// runs between another call's lookup and launch on the same stream.
+struct StreamScratch {
+  std::mutex mu;
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, std::unique_ptr<StreamScratch>> g_workspaces;  // guarded by g_mu
 
 int current_device(int* dev) {
   if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return FORGE_ERR_CUDA;
@@ -350,27 +360,42 @@ int launch_plan(DecodePlan* plan, cudaStream_t stream) {
   return FORGE_OK;
 }
 
-// Library-owned workspace for (device, stream), grown on demand.
-int cached_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  auto& slot = g_workspaces[{dev, stream}];
-  if (slot.second < bytes) {
-    if (slot.first) {
-      // the old buffer may still be in use by work queued on this stream
-      if (cudaStreamSynchronize(stream) != cudaSuccess) return FORGE_ERR_CUDA;
-      cudaFree(slot.first);
-      slot = {nullptr, 0};
-    }
+// Library-owned workspace for (device, stream), grown on demand with
+// stream-ordered allocation: the new buffer is allocated and zero-filled on
+// `stream` (the split arrival counters start at zero; kernels return them to
+// zero), and the old one is released with cudaFreeAsync on the same stream,
+// after the work already queued there.  No host synchronisation.  Growth is
+// refused while `stream` is being captured (the buffer would belong to the
+// graph).  On success `hold` owns the scratch's lock: the caller keeps it
+// until its kernel is enqueued.
+int cached_workspace(int dev, cudaStream_t stream, size_t bytes, void** out, std::unique_lock<std::mutex>* hold) {
+  StreamScratch* sc = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto& slot = g_workspaces[{dev, stream}];
+    if (!slot) slot.reset(new StreamScratch);
+    sc = slot.get();  // never removed, so the pointer stays valid
+  }
+  std::unique_lock<std::mutex> lock(sc->mu);
+  if (sc->bytes < bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FORGE_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return FORGE_ERR_WORKSPACE;
     void* p = nullptr;
-    if (cudaMalloc(&p, bytes) != cudaSuccess) return FORGE_ERR_CUDA;
-    // the split arrival counters start at zero (kernels return them to zero)
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return FORGE_ERR_CUDA;
     if (cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) {
-      cudaFree(p);
+      cudaFreeAsync(p, stream);
       return FORGE_ERR_CUDA;
     }
-    slot = {p, bytes};
+    if (sc->ptr && cudaFreeAsync(sc->ptr, stream) != cudaSuccess) {
+      cudaFreeAsync(p, stream);
+      return FORGE_ERR_CUDA;
+    }
+    sc->ptr = p;
+    sc->bytes = bytes;
   }
-  *out = slot.first;
+  *out = sc->ptr;
+  *hold = std::move(lock);
   return FORGE_OK;
 }
 
@@ -492,7 +517,9 @@ int forge_paged_gqa_decode(const forge_tensor* q, const forge_tensor* k_cache, c
   FORGE_TRY(device_state(dev, &err, &sms));
   FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, sms, &plan));
   void* ws = nullptr;
-  if (plan.ws_bytes > 0) FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws));
+  std::unique_lock<std::mutex> hold;  // the stream's scratch, held until the launch is enqueued
+  if (plan.ws_bytes > 0)
+    FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws, &hold));
   plan.p.err = err;
   attach_workspace(&plan, ws);
   return launch_plan(&plan, static_cast<cudaStream_t>(stream));
@@ -584,7 +611,9 @@ int append_decode_impl(const forge_tensor* q, const forge_tensor* k_new, const f
   FORGE_TRY(device_state(dev, &err, &sms));
   FORGE_TRY(plan_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, 0, sms, &plan));
   void* ws = nullptr;
-  if (plan.ws_bytes > 0) FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws));
+  std::unique_lock<std::mutex> hold;  // the stream's scratch, held until the launch is enqueued
+  if (plan.ws_bytes > 0)
+    FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), plan.ws_bytes, &ws, &hold));
   plan.p.err = err;
   plan.p.k_new = static_cast<const __nv_bfloat16*>(k_new->data);
   plan.p.v_new = static_cast<const __nv_bfloat16*>(v_new->data);
