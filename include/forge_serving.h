@@ -161,8 +161,9 @@ FORGE_API int forge_batch_events(const forge_batch *batch, int kind, int32_t cap
  *                 the device table after the update, or -1 for an empty row.
  * The step's description goes through a pinned staging buffer with one
  * cudaMemcpyAsync, then one single-CTA kernel; the call does not wait for
- * the device except when a staging buffer is reused before its previous
- * copy ended.  Not capturable into a CUDA graph (FORGE_ERR_UNSUPPORTED while
+ * the device except when a staging buffer (one of a ring of 4) is reused
+ * before the apply kernel that last read it has ended.  Applies of one batch
+ * may go to different streams.  Not capturable into a CUDA graph (FORGE_ERR_UNSUPPORTED while
  * the stream captures).  A batch stays on the device of its first apply
  * (FORGE_ERR_VALUE on another).  FORGE_ERR_DTYPE / FORGE_ERR_SHAPE on
  * tensors that do not match, FORGE_ERR_CUDA on a failed CUDA call.

@@ -182,7 +182,8 @@ struct Event {
 };
 
 // One pinned host buffer and its device twin; `done` is recorded after the
-// copy that read the host side.
+// apply kernel, which follows the copy that read the host side, so it marks
+// both buffers free.
 struct Stage {
   int32_t* host = nullptr;
   int32_t* dev = nullptr;
@@ -526,14 +527,17 @@ int forge_batch_apply(forge_batch* b, forge_tensor* block_tables, forge_tensor* 
   std::copy(b->stage.begin(), b->stage.end(), st.host);
   if (cudaMemcpyAsync(st.dev, st.host, words * sizeof(int32_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FORGE_ERR_CUDA;
-  if (cudaEventRecord(st.done, s) != cudaSuccess) return FORGE_ERR_CUDA;
-  st.pending = true;
-  b->ring_next = (b->ring_next + 1) % kStages;
   batch_apply_kernel<<<1, 256, 0, s>>>(st.dev, static_cast<int32_t*>(block_tables->data), block_tables->stride[0],
                                        static_cast<int32_t>(block_tables->shape[1]),
                                        static_cast<int32_t*>(context_lens->data),
                                        static_cast<int64_t*>(slot_mapping->data), b->pool->block_size);
   if (cudaGetLastError() != cudaSuccess) return FORGE_ERR_CUDA;
+  // One event after the kernel covers both of the stage's buffers: the copy
+  // has read the host buffer and the kernel has read the device buffer, so
+  // a later apply (on any stream) may refill either.
+  if (cudaEventRecord(st.done, s) != cudaSuccess) return FORGE_ERR_CUDA;
+  st.pending = true;
+  b->ring_next = (b->ring_next + 1) % kStages;
   std::fill(b->row_full.begin(), b->row_full.end(), 0);
   b->applied = true;
   return FORGE_OK;

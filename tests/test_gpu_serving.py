@@ -211,3 +211,33 @@ def test_serving_loop_matches_the_oracle(mode):
     assert np.array_equal(bits_host(kc_d), kc_h) and np.array_equal(bits_host(vc_d), vc_h)
     assert B.forge_paged_get_device_error() == 0
     assert d.close() == 0
+
+
+def test_applies_alternating_between_two_streams():
+    """Applies of one batch go to two streams in turn, ordered by events but
+    never synchronised with the host between checks, for many more steps than
+    the staging ring has buffers: a buffer is refilled only once the apply
+    kernel that last read it has ended, so the device state stays the
+    oracle's."""
+    d = Driver(300, 16, 16, 8, 512)
+    reqs = W.request_stream(60, 33, prompt_median=100.0, prompt_max=200, new_max=30, arrivals_per_step=1.0)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    retired, step, prev, checks = 0, 0, None, 0
+    while retired < len(reqs.seq_ids):
+        for req in reqs.arriving(step):
+            d.submit(req)
+        s = streams[step % 2]
+        if prev is not None:
+            s.wait_event(prev)
+        want = d.step(stream=s)
+        prev = torch.cuda.Event()
+        prev.record(s)
+        retired += len(want["retired"])
+        step += 1
+        if step % 9 == 0:               # the 8 applies before this check ran without a host sync
+            d.check_device(want)
+            checks += 1
+    d.check_device(want)
+    assert checks >= 2
+    assert d.close() == 0
