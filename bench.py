@@ -15,7 +15,13 @@ blocks interleaved in the pool, bf16 storage.
 Reported metric: decode KV-read bandwidth in GB/s (algorithmic bytes = q +
 every cached token's K and V rows + out, per step) and microseconds per
 layer-step.  Inputs are larger than L2 (the KV pool is ~0.63 GB against a
-126 MB L2), so no flush is done between steps.
+126 MB L2), so no flush is done between steps.  The dominant kernel is also
+timed on its own over at least 50 graph replays of 20 launches (p10 / p50 /
+p90 per launch), layer 0's output is checked against the oracle
+(max_abs_err), and `per_config` repeats the kernel timing and the check for
+every workload of the list (tiny, Qwen3-0.6B, skewed with fp32 and bf16
+output, the 36-layer step); workloads whose pools are smaller than 4 x L2
+rotate pool copies from launch to launch.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 Under torchrun each rank runs an independent replica of the workload on its
@@ -182,15 +188,42 @@ def _seq_bytes(wl, b, out_bytes):
     return wl.Hq * wl.D * 2 + int(wl.context_lens[b]) * wl.Hkv * wl.D * 4 + wl.Hq * wl.D * out_bytes
 
 
-def _config_dict(wl, extra=None):
+def _timing_plan(wl, steps, graphs=True):
+    """How the GPU arm times a workload, from its sizes and the run's
+    arguments only (so both arms can state it): bytes of one step's KV pools,
+    the number R of pool copies rotated step to step when those are smaller
+    than 4 x L2, the steps per captured graph, and the copies a graph uses."""
+    L = wl.layers
+    step_pool_bytes = 2 * L * wl.NB * wl.Hkv * 16 * wl.D * 2
+    R = min(64, max(1, -(-4 * L2_BYTES // step_pool_bytes)))
+    chunk = max(c for c in range(1, max(1, 20 // L) + 1) if steps % c == 0) if graphs else 1
+    copies_used = min(R, chunk) if graphs else R
+    return step_pool_bytes, R, chunk, copies_used
+
+
+def _l2_note(step_pool_bytes, R, copies_used):
+    if R == 1:
+        return f"no flush: inputs larger than L2 (KV pool {step_pool_bytes / 1e6:.0f} MB vs 126 MB L2)"
+    return (f"{copies_used} copies of the KV pools rotated step to step "
+            f"({copies_used * step_pool_bytes / 1e6:.0f} MB vs 126 MB L2)")
+
+
+def _config_dict(wl, args=None, out_bytes=None):
+    """The `config` object of the JSON line; the same for both arms."""
     s = wl.spec
     lens = wl.context_lens
     d = {"workload": f"{s.name}: {s.description}", "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv,
          "head_dim": s.D, "block_size": 16, "pool_blocks": wl.NB, "tokens": int(lens.sum()),
          "context_len_min": int(lens.min()), "context_len_max": int(lens.max()), "seed": wl.seed,
          "out_dtype": s.out_dtype, "parallelism": "replicas (one independent batch per GPU)"}
-    if extra:
-        d.update(extra)
+    if args is not None:
+        graphs = getattr(args, "graphs", True)
+        spb, R, chunk, used = _timing_plan(wl, args.steps, graphs)
+        ob = out_bytes if out_bytes is not None else (4 if s.out_dtype == "f32" else 2)
+        d.update({"launch": (f"CUDA graphs of {chunk} steps replayed" if graphs else "eager C-ABI calls"),
+                  "l2": _l2_note(spb, R, used), "layers": wl.layers,
+                  "bytes_per_step": wl.layers * wl.bytes_decode(ob),
+                  "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"})
     return d
 
 
@@ -283,7 +316,7 @@ def run_reference(args, wl, out_bytes):
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": _config_dict(wl),
+            "data": "synthetic", "config": _config_dict(wl, args, out_bytes),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -291,6 +324,207 @@ def run_reference(args, wl, out_bytes):
 
 
 # --------------------------------------------------------------------------- GPU leg
+
+PER_CONFIG = ("tiny", "qwen3_0_6b", "qwen3_4b", "skewed", "skewed_bf16", "cb36")
+TOL = {"f32": 2e-3, "bf16": 1.6e-2}   # max-abs error bound against the fp64 oracle
+
+
+class Rig:
+    """Device buffers of one workload for the timed loops.
+
+    Layers share one block table and one pool [R*L, NB, Hkv, 16, D] (R
+    identical copies, rotated step to step when one step's pools are
+    smaller than 4 x L2); each layer has its own q, new K/V row and output.
+    Layer 0 holds the seeded workload values (checked against the oracle);
+    the other layers hold them too when ``host_layers`` is "all", else
+    device-drawn N(0, 1) values with the same NaN poison (same shapes and
+    structure, faster to make)."""
+
+    def __init__(self, wl, dev, stream, steps, graphs, host_layers="all"):
+        import torch
+        self.torch, self.wl, self.dev, self.stream = torch, wl, dev, stream
+        L = wl.layers
+        self.step_pool_bytes, self.R, self.chunk, self.copies_used = _timing_plan(wl, steps, graphs)
+        self.graphs = graphs
+        self.t0 = wl.layer(0)
+        self.host = {"q": torch.empty(L, wl.B, wl.Hq, wl.D, dtype=torch.bfloat16).pin_memory(),
+                     "k_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
+                     "v_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
+                     "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+                     "tables": torch.from_numpy(wl.block_tables).pin_memory(),
+                     "lens": torch.from_numpy(wl.context_lens).pin_memory()}
+        R = self.R
+        self.pool_k = torch.empty(R * L, wl.NB, wl.Hkv, 16, wl.D, dtype=torch.bfloat16, device=dev)
+        self.pool_v = torch.empty_like(self.pool_k)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed)
+        pb, po = np.nonzero(wl.poison_mask())
+        pb_d, po_d = torch.from_numpy(pb).to(dev), torch.from_numpy(po).to(dev)
+        for layer in range(L):
+            if layer == 0 or host_layers == "all":
+                t = self.t0 if layer == 0 else wl.layer(layer)
+                for k in ("q", "k_new", "v_new"):
+                    self.host[k][layer].copy_(_bf(torch, t[k]))
+                self.pool_k[layer].copy_(_bf(torch, t["k_cache"]))
+                self.pool_v[layer].copy_(_bf(torch, t["v_cache"]))
+            else:
+                for k in ("q", "k_new", "v_new"):
+                    self.host[k][layer].copy_(torch.randn(self.host[k].shape[1:], generator=gen, device=dev)
+                                              .to(torch.bfloat16).cpu())
+                for pool in (self.pool_k, self.pool_v):
+                    pool[layer].normal_(generator=gen)
+                    pool[layer][pb_d, :, po_d, :] = float("nan")
+        for r in range(1, R):
+            self.pool_k[r * L:(r + 1) * L].copy_(self.pool_k[:L])
+            self.pool_v[r * L:(r + 1) * L].copy_(self.pool_v[:L])
+        self.rot = 0
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        self.out_dt = torch.bfloat16 if wl.spec.out_dtype == "bf16" else torch.float32
+        self.d["out"] = torch.empty(L, wl.B, wl.Hq, wl.D, dtype=self.out_dt, device=dev)
+        self.qw, self.kw = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+                            for a in wl.qk_norm_weights(0))
+        self.rope_table = None
+
+    def next_copy(self):
+        r = self.rot
+        self.rot = (r + 1) % self.R
+        return r * self.wl.layers
+
+    # one step of each path over every layer (the step functions read their
+    # buffers from self.d at call time: the end-to-end loop swaps them)
+    def step_fused(self):
+        from paged_kv_gqa_06_gb300 import binding as B
+        d, wl, base = self.d, self.wl, self.next_copy()
+        for layer in range(wl.layers):
+            B.forge_paged_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer],
+                                            self.pool_k[base + layer], self.pool_v[base + layer], d["tables"],
+                                            d["lens"], wl.scale, d["out"][layer], stream=self.stream)
+
+    def step_separate(self):
+        from paged_kv_gqa_06_gb300 import binding as B
+        d, wl, base = self.d, self.wl, self.next_copy()
+        for layer in range(wl.layers):
+            B.forge_paged_kv_append(d["k_new"][layer], d["v_new"][layer], d["slots"], self.pool_k[base + layer],
+                                    self.pool_v[base + layer], stream=self.stream)
+            B.forge_paged_gqa_decode(d["q"][layer], self.pool_k[base + layer], self.pool_v[base + layer],
+                                     d["tables"], d["lens"], wl.scale, d["out"][layer], stream=self.stream)
+
+    def step_decode_only(self):
+        from paged_kv_gqa_06_gb300 import binding as B
+        d, wl, base = self.d, self.wl, self.next_copy()
+        for layer in range(wl.layers):
+            B.forge_paged_gqa_decode(d["q"][layer], self.pool_k[base + layer], self.pool_v[base + layer],
+                                     d["tables"], d["lens"], wl.scale, d["out"][layer], stream=self.stream)
+
+    def step_qk(self):
+        """The q/k path (per-head RMSNorm + RoPE on q and the new k) in the same launch."""
+        from paged_kv_gqa_06_gb300 import binding as B
+        if self.rope_table is None:
+            self.rope_table = B.forge_rope_cos_sin_table(1e6, self.wl.D, self.wl.MB * 16).to(self.dev)
+        d, wl, base = self.d, self.wl, self.next_copy()
+        for layer in range(wl.layers):
+            B.forge_paged_qk_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer],
+                                               self.pool_k[base + layer], self.pool_v[base + layer], d["tables"],
+                                               d["lens"], wl.scale, d["out"][layer], q_norm_weight=self.qw,
+                                               k_norm_weight=self.kw, norm_eps=1e-6, rope_cos_sin=self.rope_table,
+                                               stream=self.stream)
+
+    def runner(self, fn, n):
+        """A callable that runs `fn` n times: one CUDA graph replay (or eager calls)."""
+        torch = self.torch
+        if not self.graphs:
+            def eager():
+                for _ in range(n):
+                    fn()
+            return eager
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                for _ in range(n):
+                    fn()
+        return g.replay
+
+    def timed(self, run, n, per_call_events=False):
+        """Device time (ms) of n runs on the stream: one total, or one per run."""
+        torch = self.torch
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range((n if per_call_events else 1) + 1)]
+        with torch.cuda.stream(self.stream):
+            ev[0].record(self.stream)
+            for r in range(n):
+                run()
+                if per_call_events:
+                    ev[r + 1].record(self.stream)
+            if not per_call_events:
+                ev[1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
+
+    def sample_launches(self, fn, launches_per_call, min_samples=50, min_seconds=0.4, per_sample=20):
+        """Per-launch device times (ms) of `fn` (one step: launches_per_call
+        kernel launches): graph replays of ceil(per_sample / launches_per_call)
+        steps each, timed one replay at a time with events on the stream, at
+        least min_samples replays and min_seconds in all."""
+        reps = max(1, -(-per_sample // launches_per_call))
+        run = self.runner(fn, reps)
+        self.timed(run, 3)                                  # warm
+        est = self.timed(run, 5)[0] / 5
+        n = max(min_samples, int(math.ceil(min_seconds * 1e3 / max(est, 1e-3))))
+        per = self.timed(run, n, per_call_events=True)
+        return [x / (reps * launches_per_call) for x in per], n * reps * launches_per_call
+
+    def layer0_check(self):
+        """What the CPU-baseline leg needs to check layer 0's output against
+        the oracle: the workload, layer 0's inputs and the GPU output (host)."""
+        return (self.wl, self.t0, self.d["out"][0].detach().double().cpu().numpy())
+
+
+def _bf(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def _pcts(ms):
+    return [round(float(np.percentile(ms, q)) * 1e3, 2) for q in (10, 50, 90)]
+
+
+def measure_config(name, dev, stream):
+    """One per_config entry: the fused step of workload `name` (one append +
+    decode launch per layer) timed over at least 50 graph replays of at least
+    20 launches, its bandwidth against the HBM peak, and layer 0's output
+    against the oracle."""
+    import torch
+
+    from paged_kv_gqa_06_gb300 import binding
+    from paged_kv_gqa_06_gb300 import workloads as W
+
+    wl = W.make_workload(name)
+    ob = 4 if wl.spec.out_dtype == "f32" else 2
+
+    rig = Rig(wl, dev, stream, 20, True, host_layers="first")
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            rig.step_fused()                         # sizes the split scratch before capture
+    stream.synchronize()
+    assert binding.forge_paged_get_device_error(stream) == 0
+    check = rig.layer0_check()                       # the output of a fused step (append, then decode)
+    w0 = time.time()
+    per_launch, launches = rig.sample_launches(rig.step_fused, wl.layers)
+    w1 = time.time()
+    peak, _ = _peaks()
+    bytes_layer = wl.bytes_decode(ob)
+    mean_ms = statistics.fmean(per_launch)
+    split, kern = binding.forge_paged_gqa_decode_plan(wl.B, wl.Hkv, wl.MB)
+    entry = {"workload": f"{name}: {wl.spec.description}", "tokens": int(wl.context_lens.sum()),
+             "layers": wl.layers, "kernel": DECODE_KERNELS[kern], "split_tokens": split,
+             "us_per_layer_step": round(mean_ms * 1e3, 2), "us_p10_p50_p90": _pcts(per_launch),
+             "gbs": round(bytes_layer / (mean_ms * 1e-3) / 1e9, 1),
+             "frac": round(bytes_layer / (mean_ms * 1e-3) / 1e9 / peak, 4),
+             "launches_timed": launches, "samples": len(per_launch),
+             "l2": _l2_note(rig.step_pool_bytes, rig.R, min(rig.R, max(1, -(-20 // wl.layers)))),
+             "max_abs_err": None, "tol": TOL[wl.spec.out_dtype], "out_dtype": wl.spec.out_dtype}
+    del rig
+    torch.cuda.empty_cache()
+    return entry, (w0, w1), check
+
 
 def run_native(args, wl, out_bytes):
     import torch
@@ -306,103 +540,16 @@ def run_native(args, wl, out_bytes):
     torch.cuda.set_device(dev)
     binding.load_library()
 
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-
-    # Layers share one block table and one pool [L, NB, Hkv, 16, D]; each
-    # layer has its own q, new K/V row and output.  Single-layer workloads
-    # are the L = 1 case.
-    L = wl.layers
-    host = {"q": torch.empty(L, wl.B, wl.Hq, wl.D, dtype=torch.bfloat16).pin_memory(),
-            "k_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
-            "v_new": torch.empty(L, wl.B, wl.Hkv, wl.D, dtype=torch.bfloat16).pin_memory(),
-            "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
-            "tables": torch.from_numpy(wl.block_tables).pin_memory(),
-            "lens": torch.from_numpy(wl.context_lens).pin_memory()}
-    # When one step's K/V pools are smaller than 4 x L2, successive steps
-    # rotate over R identical copies of them, so that every step reads its
-    # K/V from HBM (the appends write the same row into every copy).
-    step_pool_bytes = 2 * L * wl.NB * wl.Hkv * 16 * wl.D * 2
-    R = min(64, max(1, -(-4 * L2_BYTES // step_pool_bytes)))
-    pool_k = torch.empty(R * L, wl.NB, wl.Hkv, 16, wl.D, dtype=torch.bfloat16, device=dev)
-    pool_v = torch.empty_like(pool_k)
-    for layer in range(L):
-        t = wl.layer(layer)
-        for k in ("q", "k_new", "v_new"):
-            host[k][layer].copy_(bf(t[k]))
-        pool_k[layer].copy_(bf(t["k_cache"]))
-        pool_v[layer].copy_(bf(t["v_cache"]))
-        del t
-    for r in range(1, R):
-        pool_k[r * L:(r + 1) * L].copy_(pool_k[:L])
-        pool_v[r * L:(r + 1) * L].copy_(pool_v[:L])
-    rot = [0]  # the copy the next step uses
-
-    def next_copy():
-        r = rot[0]
-        rot[0] = (r + 1) % R
-        return r * L
-    d = {k: v.to(dev) for k, v in host.items()}
-    out_dt = torch.bfloat16 if wl.spec.out_dtype == "bf16" else torch.float32
-    out = torch.empty(L, wl.B, wl.Hq, wl.D, dtype=out_dt, device=dev)
-
     stream = torch.cuda.Stream(device=dev)
+    rig = Rig(wl, dev, stream, args.steps, args.graphs, host_layers="all")
+    L = wl.layers
     bytes_layer = wl.bytes_decode(out_bytes)
     bytes_step = L * bytes_layer
-    launches_per_step = 2 * L  # append + decode per layer (the split merge runs inside the decode kernel)
-
-    d["out"] = out  # the step functions read their buffers from d at call time (the end-to-end loop swaps them)
-
-    def decode(layer, base):
-        binding.forge_paged_gqa_decode(d["q"][layer], pool_k[base + layer], pool_v[base + layer], d["tables"],
-                                       d["lens"], wl.scale, d["out"][layer], stream=stream)
-
-    def append(layer, base):
-        binding.forge_paged_kv_append(d["k_new"][layer], d["v_new"][layer], d["slots"], pool_k[base + layer],
-                                      pool_v[base + layer], stream=stream)
-
-    def fused(layer, base):
-        binding.forge_paged_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer],
-                                              pool_k[base + layer], pool_v[base + layer], d["tables"], d["lens"],
-                                              wl.scale, d["out"][layer], stream=stream)
-
-    # the q/k path (per-head RMSNorm + RoPE on q and the new k) in the same launch
-    qw, kw = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for a in wl.qk_norm_weights(0))
-    rope_table = binding.forge_rope_cos_sin_table(1e6, wl.D, wl.MB * 16).to(dev)
-
-    def fused_qk(layer, base):
-        binding.forge_paged_qk_append_gqa_decode(d["q"][layer], d["k_new"][layer], d["v_new"][layer],
-                                                 pool_k[base + layer], pool_v[base + layer], d["tables"], d["lens"],
-                                                 wl.scale, d["out"][layer], q_norm_weight=qw, k_norm_weight=kw,
-                                                 norm_eps=1e-6, rope_cos_sin=rope_table, stream=stream)
-
-    def step_qk():
-        base = next_copy()
-        for layer in range(L):
-            fused_qk(layer, base)
-
-    def step_separate():  # the two entry points: append, then decode, per layer
-        base = next_copy()
-        for layer in range(L):
-            append(layer, base)
-            decode(layer, base)
-
-    def step_fused():  # one launch per layer
-        base = next_copy()
-        for layer in range(L):
-            fused(layer, base)
-
-    def decode_only():
-        base = next_copy()
-        for layer in range(L):
-            decode(layer, base)
-
-    paths = {"fused": step_fused, "separate": step_separate, "qk": step_qk}
+    paths = {"fused": rig.step_fused, "separate": rig.step_separate, "qk": rig.step_qk}
     step = paths[args.path]
     others = {k: v for k, v in paths.items() if k != args.path}
-    kernel_only = decode_only if args.path == "separate" else step
+    kernel_only = rig.step_decode_only if args.path == "separate" else step
     launches_per_step = 2 * L if args.path == "separate" else L
-
 
     with torch.cuda.stream(stream):
         for _ in range(3):  # eager calls first: the decode sizes its workspace on this stream
@@ -415,38 +562,12 @@ def run_native(args, wl, out_bytes):
     # the way a serving loop replays a captured decode step: no Python or
     # per-call launch overhead between kernels.  With --no-graphs the loops
     # make eager C-ABI calls instead.
-    chunk = max(c for c in range(1, max(1, 20 // L) + 1) if args.steps % c == 0) if args.graphs else 1
-
-    def runner(fn):
-        if not args.graphs:
-            return fn
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(chunk):
-                    fn()
-        return g.replay
-
-    run_step, run_kernel = runner(step), runner(kernel_only)
-    copies_used = min(R, chunk) if args.graphs else R  # a graph replays the copies it captured
-    run_others = {k: runner(v) for k, v in others.items()}
+    chunk = rig.chunk
+    run_step = rig.runner(step, chunk)
+    run_others = {k: rig.runner(v, chunk) for k, v in others.items()}
     reps = args.steps // chunk
-
-    def timed(run, n, per_call_events=False):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range((n if per_call_events else 1) + 1)]
-        with torch.cuda.stream(stream):
-            ev[0].record(stream)
-            for r in range(n):
-                run()
-                if per_call_events:
-                    ev[r + 1].record(stream)
-            if not per_call_events:
-                ev[1].record(stream)
-        torch.cuda.synchronize(dev)
-        return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
-
-    for run in (run_step, run_kernel, *run_others.values()):
-        timed(run, max(3, args.warmup) // chunk + 1)
+    for run in (run_step, *run_others.values()):
+        rig.timed(run, max(3, args.warmup) // chunk + 1)
 
     # ---------------- timed region (device-resident inputs)
     sampler = ClockSampler(_gpu_id(torch, dev.index or 0)) if rank == 0 else None
@@ -455,19 +576,37 @@ def run_native(args, wl, out_bytes):
         dist.barrier()
     torch.cuda.synchronize(dev)
     w0 = time.time()
-    ms_total = timed(run_step, reps)[0]
+    ms_total = rig.timed(run_step, reps)[0]
     w1 = time.time()
     if ws > 1:
         dist.barrier()
+
+    # ---------------- the dominant kernel alone: at least 50 samples of at
+    # least 20 launches (graph replays, events on its stream), whatever --steps is
+    decode_ms, dec_launches = rig.sample_launches(kernel_only, L, min_samples=args.kernel_samples,
+                                                  min_seconds=0.4 if args.kernel_samples >= 50 else 0.0)
+    w2 = time.time()
+    # layer 0's output of the timed kernel, for the oracle check (the q/k path
+    # computes another function: RMSNorm and RoPE first)
+    checks = {wl.spec.name: rig.layer0_check()} if args.path != "qk" else {}
+
+    # ---------------- the other ways of running the step, for comparison
+    ms_others = {k: rig.timed(r, reps)[0] for k, r in run_others.items()}
+
+    # ---------------- every configuration of the workload list, one after another
+    per_config = {}
+    if rank == 0 and ws == 1 and args.per_config:
+        windows = {}
+        for name in PER_CONFIG:
+            if name == wl.spec.name:
+                continue
+            per_config[name], windows[name], checks[name] = measure_config(name, dev, stream)
     rows = sampler.stop() if sampler else []
-    clocks = ClockSampler.summarize(rows, w0, w1) if sampler else None
-
-    # ---------------- the other way of running the step, for comparison
-    ms_others = {k: timed(r, reps)[0] for k, r in run_others.items()}
-
-    # ---------------- the dominant kernel alone, same launch path, events on its stream
-    dec_reps = max(1, min(reps, 2000 // chunk))
-    decode_ms = [x / (chunk * L) for x in timed(run_kernel, dec_reps, per_call_events=True)]
+    clocks = ClockSampler.summarize(rows, w0, w2) if sampler else None
+    if clocks is not None:
+        clocks["window"] = "timed region + dominant-kernel loop" if clocks["samples"] else clocks["window"]
+    for name, (a, b) in (windows.items() if per_config else []):
+        per_config[name]["sm_mhz"] = ClockSampler.summarize(rows, a, b)["sm_mhz"]
 
     # ---------------- end to end: host buffers, copies inside the timed region
     # Every step uploads its inputs from pinned host memory (one packed
@@ -475,6 +614,8 @@ def run_native(args, wl, out_bytes):
     # to pinned host memory.  Uploads and read-backs run on their own streams
     # with two device buffer sets, so step i+1's upload and step i-1's
     # read-back overlap step i's compute, as a serving loop would run them.
+    host, d, out = rig.host, rig.d, rig.d["out"]
+    out_dt = rig.out_dt
     fields = ("q", "k_new", "v_new", "slots", "tables", "lens")
     nbytes = {k: host[k].numel() * host[k].element_size() for k in fields}
     offs, total = {}, 0
@@ -558,19 +699,16 @@ def run_native(args, wl, out_bytes):
     traffic = _traffic_from_profile(_decode_source_hash(), kern) if wl.spec.name == "qwen3_4b" else None
     h2d = total  # the packed input buffer, as copied each step
     d2h = host_out.numel() * host_out.element_size()
+    tol = TOL[wl.spec.out_dtype]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "us_per_layer_step": round(ms_step * 1e3 / L, 2),
         "pct_of_hbm_peak": round(100.0 * value / ws / peak, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
-        "config": _config_dict(wl, {"launch": (f"CUDA graphs of {chunk} steps (append + decode) replayed"
-                                               if args.graphs else "eager C-ABI calls"),
-                                    "l2": ("no flush: inputs larger than L2 (KV pool "
-                                           f"{step_pool_bytes / 1e6:.0f} MB vs 126 MB L2)" if R == 1 else
-                                           f"{copies_used} copies of the KV pools rotated step to step "
-                                           f"({copies_used * step_pool_bytes / 1e6:.0f} MB vs 126 MB L2)"),
-                                    "layers": L, "bytes_per_step": bytes_step,
-                                    "bytes_rule": "q + K/V rows of every cached token + out (token-exact)"}),
+        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+        "arithmetic": "bf16 operands on the tensor cores (softmax weights as bf16 high + low parts), fp32 "
+                      "accumulation, softmax and split merge in fp32",
+        "data": "synthetic",
+        "config": _config_dict(wl, args, out_bytes),
         "roofline": {"bound": "hbm",
                      "kernel": (f"{DECODE_KERNELS[kern]} (one decode call; split merge inside)"
                                 if args.path == "separate" else
@@ -579,9 +717,10 @@ def run_native(args, wl, out_bytes):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "decode_us": round(dec_avg_ms * 1e3, 2),
-                     "decode_us_p10_p50_p90": [round(float(np.percentile(decode_ms, q)) * 1e3, 2)
-                                               for q in (10, 50, 90)],
+                     "decode_us_p10_p50_p90": _pcts(decode_ms),
+                     "launches_timed": dec_launches, "samples": len(decode_ms),
                      "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src},
+        "max_abs_err": None, "tol": tol,
         "e2e": {"value": round(aggregate_gbs(ws, bytes_step, args.steps, e2e_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / args.steps, 5),
@@ -596,9 +735,34 @@ def run_native(args, wl, out_bytes):
                         for k, v in ms_others.items()},
         "clocks": clocks,
     }
+    if per_config:
+        head = {"workload": line["config"]["workload"], "tokens": line["config"]["tokens"], "layers": L,
+                "kernel": DECODE_KERNELS[kern], "split_tokens": split_tokens,
+                "us_per_layer_step": round(dec_avg_ms * 1e3, 2), "us_p10_p50_p90": _pcts(decode_ms),
+                "gbs": round(achieved, 1), "frac": round(achieved / peak, 4), "launches_timed": dec_launches,
+                "samples": len(decode_ms), "l2": line["config"]["l2"], "max_abs_err": None, "tol": tol,
+                "out_dtype": wl.spec.out_dtype, "sm_mhz": clocks["sm_mhz"] if clocks else None}
+        per_config = {wl.spec.name: head, **per_config}
+        line["per_config"] = {k: per_config[k] for k in PER_CONFIG if k in per_config}
+    line["_checks"] = checks   # filled into max_abs_err by the CPU-baseline leg, then dropped
     if ws > 1:
         dist.destroy_process_group()
     return line
+
+
+def check_outputs(line, checks):
+    """CPU-baseline leg: layer 0's GPU output of every timed workload against
+    the oracle on the same inputs (max-abs error, in the line and per_config)."""
+    import oracle
+    for name, (wl, t, got) in checks.items():
+        kc, vc = t["k_cache"].copy(), t["v_cache"].copy()
+        oracle.paged_kv_append(t["k_new"], t["v_new"], wl.slot_mapping, kc, vc)
+        ref = oracle.paged_gqa_decode(t["q"], kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+        err = float(np.max(np.abs(got - ref))) if np.all(np.isfinite(got)) else float("inf")
+        if name == line["config"]["workload"].split(":")[0]:
+            line["max_abs_err"] = err
+        if name in line.get("per_config", {}):
+            line["per_config"][name]["max_abs_err"] = err
 
 
 def run_serving(args, wl):
@@ -870,6 +1034,11 @@ def main(argv=None):
                     help="time eager C-ABI calls instead of replaying captured steps")
     ap.add_argument("--prefill", action="store_true",
                     help="time the paged prefill on a prefill workload (default prefill_4b)")
+    ap.add_argument("--kernel-samples", type=int, default=50,
+                    help="graph replays (of 20 launches) timing the dominant kernel; below 50 (for profiler "
+                         "runs) there is no minimum duration either")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip timing the other workloads of the list (per_config in the line)")
     ap.add_argument("--serving", action="store_true",
                     help="continuous batching through the block pool + batch driver (multi-layer workloads)")
     args = ap.parse_args(argv)
@@ -908,8 +1077,10 @@ def main(argv=None):
     line = run_native(args, wl, out_bytes)
     if line is None:
         return 0
+    checks = line.pop("_checks")
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, out_bytes)
+        check_outputs(line, checks)
     print(json.dumps(line), flush=True)
     return 0
 

@@ -95,3 +95,44 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0 and cb["cores"] >= 1
     st = cb["single_thread"]
     assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "GB/s"
+
+
+def test_output_check_of_the_cpu_leg_reports_max_abs_error():
+    """check_outputs (run in the CPU-baseline leg) puts each workload's
+    max-abs error against the oracle into the line and its per_config entry."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    from paged_kv_gqa_06_gb300 import workloads as W
+    wl = W.make_workload("tiny")
+    t = wl.layer(0)
+    kc, vc = t["k_cache"].copy(), t["v_cache"].copy()
+    oracle.paged_kv_append(t["k_new"], t["v_new"], wl.slot_mapping, kc, vc)
+    ref = oracle.paged_gqa_decode(t["q"], kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    got = ref.copy()
+    got[1, 2, 3] += 1e-3
+    line = {"config": {"workload": "tiny: x"}, "max_abs_err": None, "per_config": {"tiny": {"max_abs_err": None}}}
+    bench.check_outputs(line, {"tiny": (wl, t, got)})
+    assert line["max_abs_err"] == pytest.approx(1e-3, rel=1e-9)
+    assert line["per_config"]["tiny"]["max_abs_err"] == line["max_abs_err"]
+    got[0, 0, 0] = np.nan
+    bench.check_outputs(line, {"tiny": (wl, t, got)})
+    assert line["max_abs_err"] == float("inf")
+
+
+def test_reference_arm_has_the_gpu_arms_config():
+    """Both arms state the same config (workload, sizes, launch and L2 handling)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_gqa_06_gb300 import workloads as W
+    wl = W.make_workload("qwen3_4b")
+
+    class Args:
+        steps, warmup, graphs = 20, 5, True
+    cfg = bench._config_dict(wl, Args(), 2)
+    assert cfg["l2"].startswith("no flush") and cfg["launch"] == "CUDA graphs of 20 steps replayed"
+    assert cfg["bytes_per_step"] == wl.bytes_decode(2) and cfg["layers"] == 1
+    small = bench._config_dict(W.make_workload("qwen3_0_6b"), Args(), 2)
+    assert "copies of the KV pools rotated" in small["l2"]
