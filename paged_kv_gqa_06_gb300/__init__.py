@@ -1,13 +1,14 @@
 """Paged-KV decode attention for GB300 (sm_103a).
 
-Two operations, implemented as hand-written CUDA kernels behind a C ABI
+The operations, implemented as hand-written CUDA kernels behind a C ABI
 (``include/forge_paged.h``, ``libforge_paged.so``):
 
   * ``forge_paged_kv_append`` -- scatter each sequence's new K/V token into
     its slot of the paged block pool;
   * ``forge_paged_gqa_decode`` -- grouped-query attention of one new query
     token per sequence over that sequence's cached K/V, read through its
-    block table, with split-K partials merged by a reduce kernel;
+    block table; long contexts are cut into splits whose partial results
+    the last split to finish merges, in the same launch;
   * ``forge_paged_prefill`` -- causal attention of a run of new query tokens
     per sequence (a prompt, or the next chunk of one) over the paged cache;
   * ``forge_kv_pool_*`` / ``forge_batch_*`` (``include/forge_serving.h``) --

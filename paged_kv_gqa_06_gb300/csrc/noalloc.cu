@@ -1,15 +1,15 @@
 // forge_paged_gqa_decode_noalloc: the paged GQA decode for callers that must
 // not allocate device memory.
 //
-// Some callers cannot call cudaMalloc at the point where they decode: code that
-// runs while a stream is being captured into a CUDA graph (cudaMalloc is not a
-// stream operation and synchronises, so capture forbids it), and processes
-// that size their device memory once at start-up -- for example a serving loop
-// that has handed everything left to its KV-cache pool -- and treat any later
-// allocation as a failure.  forge_paged_gqa_decode may allocate its split
-// scratch on first use; this entry point never does.  Its scratch is the
-// file-scope array below, which every GPU that loads this module holds for
-// the life of the process.
+// Some callers cannot allocate device memory at the point where they decode:
+// processes that size their device memory once at start-up -- for example a
+// serving loop that has handed everything left to its KV-block pool, where a
+// later allocation fails or takes memory the pool counts on -- and callers
+// that run under a memory manager of their own (an embedding runtime or a
+// framework allocator) that forbids allocations it did not make.
+// forge_paged_gqa_decode may allocate its split scratch on first use; this
+// entry point never does.  Its scratch is the file-scope array below, which
+// every GPU that loads this module holds for the life of the process.
 #include <cuda_runtime.h>
 
 #include <mutex>

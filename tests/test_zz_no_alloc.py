@@ -1,8 +1,10 @@
 """forge_paged_gqa_decode_noalloc: the decode for callers that cannot allocate.
 
-Such callers -- code running under CUDA-graph stream capture, or a process
-whose device memory was fixed at start-up -- call this entry point instead of
-forge_paged_gqa_decode, which may cudaMalloc its split scratch on first use.
+Such callers -- a process whose device memory was fixed at start-up (a
+serving loop that gave the rest to its KV-block pool), or code running under
+a memory manager of its own that forbids allocations it did not make -- call
+this entry point instead of forge_paged_gqa_decode, which may allocate its
+split scratch on first use.
 This test calls it through the C ABI twice in a row (the static scratch keeps
 the first call's contents) and checks both results against the regular entry
 point's within the parity tolerance.  It lives in a file of its own that
