@@ -311,14 +311,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// d = a + b on both lanes of a float pair with one packed fp32 add.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Round two floats to bf16 (hi, packed low/high = x0/x1) and the residuals
-// x - hi to bf16 (lo): hi + lo carries ~16 significant bits.
+// x - hi to bf16 (lo): hi + lo carries ~16 significant bits.  The residual
+// is exact in fp32 (x and its bf16 rounding share the leading bits).
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 r = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&r);
+  const float2 r = ffma2(make_float2(bf16lo(hi), bf16hi(hi)), make_float2(-1.f, -1.f), make_float2(x0, x1));
+  const __nv_bfloat162 rl = __floats2bfloat162_rn(r.x, r.y);
+  lo = *reinterpret_cast<const uint32_t*>(&rl);
 }
 
 // A (block, head) K or V tile of 16 tokens x D bf16 in shared memory, as the

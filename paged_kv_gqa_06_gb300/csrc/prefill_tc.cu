@@ -6,39 +6,42 @@
 // p = L_b - n_b + i and attends to every cached position t <= p of its KV
 // head's group.
 //
-// One CTA per (query tile, KV head g); a query tile is M = 128 MMA rows:
-// 128 / G consecutive query tokens x the G heads of group g (row r is token
-// r / G, head g*G + r % G).  Six warps with fixed roles:
-//   * warp 4 (producer) loads the Q tile once (a 3-D TMA box of 64 dims x G
-//     heads x 128/G tokens, which lands as 128 K-major rows) and streams the
-//     sequence's K and V, 64 tokens (4 blocks) per stage, through the block
-//     table into a 3-stage ring, up to the tile's last query position.  The
-//     third stage is the Q tile's own space, filled once Q is in TMEM;
-//   * warps 0-3 (softmax) own one row each (warp w reads TMEM lanes
-//     32w..32w+31).  First each thread copies its row of Q from shared memory
-//     into TMEM, where it is the A operand of every QK^T.  Per tile: load the
-//     row of S, mask by position (only on tiles that reach past the row's
-//     position), and keep a running maximum that only moves when the row's
-//     maximum grows by more than 8 in log2 units, so the weights stay <= 2^8
-//     and O in TMEM is rescaled rarely.  The weights P = 2^(scale s - m) are
-//     stored over the row's S in TMEM, two per column in its first 32
-//     columns, as bf16 high and low parts (low in the next 32 columns; two
-//     MMAs keep ~16 bits of each weight, as in the decode).  A weight rounded
-//     to bf16 once would lose up to 2^-8 of itself, which at |V| near 8 is as
-//     large as a bf16 output's own rounding.  At the end O is divided by the
-//     row sum and stored;
-//   * warp 5 (MMA) owns 256 TMEM columns: S (64), Q (D / 2: two bf16 per
-//     column) and the output accumulator O (D).  Its lane 0 issues
-//     S_j = Q K_j^T (M 128, N 64, K = D; Q from TMEM, K K-major straight from
-//     the TMA layout) and O += P_j V_j (M 128, N = D, K 64; P from TMEM over
-//     S, V MN-major as it lies in the stage), each as soon as its inputs are
-//     ready: S_{j+1} overwrites S, so it waits for P_j V_j.  tcgen05.commit on
-//     mbarriers tracks completion and frees stages.  With Q in TMEM, QK^T
-//     reads only K from shared memory: on this GPU an MMA with both operands
-//     in shared memory runs at well under the rate of one with A in TMEM.
-// Shared memory is 98 KB and TMEM 256 columns per CTA, so two CTAs share an
-// SM: while one CTA's softmax runs, the other's MMAs keep the tensor cores
-// busy.
+// One CTA per SM-sized piece of work: a pair of query tiles of the same
+// (sequence, KV head g).  A query tile is M = 128 MMA rows: 128 / G
+// consecutive query tokens x the G heads of group g (row r is token r / G,
+// head g*G + r % G); the second tile holds the next 128 / G tokens.  Both
+// tiles read the same K/V stream, so each K/V byte crosses from L2 once per
+// 256 query rows.  Ten warps with fixed roles:
+//   * warp 8 (producer) loads the two Q tiles once (3-D TMA boxes of 64 dims
+//     x G heads x 128/G tokens, which land as 128 K-major rows each) and
+//     streams the sequence's K and V, 128 tokens (8 blocks) per stage,
+//     through the block table into a 3-stage K ring and a 2-stage V ring, up
+//     to the pair's last query position; K runs a stage ahead of V, since
+//     S = Q K^T of a stage comes before its P V;
+//   * warp 9 (MMA) owns all 512 TMEM columns: O_0, O_1 (D columns each at
+//     0 and 128) and S_0, S_1 (128 columns each at 256 and 384).  Its lane 0
+//     issues S_t = Q_t K_j^T (M 128, N 128, K = D; both operands K-major in
+//     shared memory as TMA wrote them) and O_t += P_t V_j (M 128, N = D,
+//     K 128; P from TMEM over S_t, V MN-major as it lies in the stage).  The
+//     order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1) keeps one tile's MMAs
+//     running while the other tile's softmax works.  S_t is rewritten only
+//     after the P_t V that reads it has completed (tcgen05.commit on
+//     mbarriers tracks completion and frees stages);
+//   * warps 0-3 and 4-7 are the softmax warpgroups of tiles 0 and 1: one row
+//     per thread, warp w reading TMEM lanes 32 (w % 4) .. +31.  Per stage:
+//     load the row of S, mask by position (only on stages that reach past
+//     the row's position), and keep a running maximum that moves only when
+//     the row's maximum grows by more than 8 in log2 units, so the weights
+//     stay <= 2^8 and O is rescaled rarely (O_t is idle then: the previous
+//     P_t V has completed before S_t was written).  The row is read twice
+//     from TMEM, for its maximum and then 32 tokens at a time for the
+//     weights, which keeps the registers of 320 threads within the SM.  The
+//     weights P = 2^(scale s - m) go over the 32 columns of S they came from,
+//     as bf16 high parts (16 columns, two weights per column) and low parts
+//     (the next 16), so P V keeps ~16 bits of each weight: a weight rounded
+//     to bf16 once could move a bf16 output by as much as its own rounding.
+//     At the end O is divided by the row sum and stored.
+// Shared memory is 225 KB (D = 128) and TMEM 512 columns, one CTA per SM.
 // V rows that may hold anything (the tail of the last block, or blocks the
 // last stage did not load) are zeroed before P V reads them: P is 0 there,
 // but 0 * NaN is NaN.  Every mbarrier wait is bounded; the MMA warp drains
@@ -51,51 +54,52 @@
 namespace forge {
 namespace {
 
-constexpr int kTcRows = 128;                 // MMA M
-constexpr int kTcKv = 64;                    // tokens per stage (MMA N of S, K of P V)
-constexpr int kTcStages = 3;                 // K/V ring depth: 2 stages + the Q tile's space once Q is in TMEM
-constexpr int kTcThreads = 6 * 32;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kTmemCols = 256;
-constexpr int kColS = 0;                     // S (and P over it): 64 columns
-constexpr int kColQ = 64;                    // Q, the A operand of QK^T: D / 2 columns (2 bf16 each)
-constexpr int kColO = 128;                   // O: D columns
+constexpr int kTcRows = 128;                 // MMA M: rows of one query tile
+constexpr int kTcTiles = 2;                  // query tiles per CTA
+constexpr int kTcKv = 128;                   // tokens per K/V stage (MMA N of S, K of P V)
+constexpr int kTcKStages = 3;                // K ring depth: K runs ahead of V
+constexpr int kTcVStages = 2;                // V ring depth
+constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
+constexpr int kTcProducerWarp = kTcSoftmaxWarps;
+constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
+constexpr int kTcThreads = (kTcSoftmaxWarps + 2) * 32;
+constexpr int kTmemCols = 512;
+constexpr int kColO = 0;                     // O_t at kColO + 128 t (D columns)
+constexpr int kColS = 256;                   // S_t (and P_t over it) at kColS + 128 t
 constexpr float kRescaleSlack = 8.0f;        // log2 units: weights stay <= 2^8
 constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kMinSmem = 116 * 1024;         // > half an SM's shared memory: one CTA per SM
 
 struct TcLayout {
-  int q, kv, bars, total;
+  int q, k, v, bars, total;
 };
 
-// Q [BOXES][128 rows][128 B] | 2 x ([K: BOXES][64][128 B], [V: same]) |
-// mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.  The third
-// K/V stage uses Q's space once Q has been copied into TMEM.
+// Q [tile][box][128 rows][128 B] | K ring [stage][box][128 tok][128 B] |
+// V ring (same) | mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.
+__host__ __device__ constexpr int q_tile_bytes(int D) { return (D / 64) * kTcRows * 128; }
+__host__ __device__ constexpr int kv_stage_bytes(int D) { return (D / 64) * kTcKv * 128; }
 __host__ __device__ constexpr TcLayout tc_layout(int D) {
-  const int boxes = D / 64;
   TcLayout l{};
   l.q = 0;
-  l.kv = l.q + boxes * kTcRows * 128;
-  l.bars = l.kv + 2 * 2 * boxes * kTcKv * 128;  // stages 0 and 1; stage 2 reuses Q's space
-  l.total = l.bars + 16 * 8 + 1024;          // barriers + slot, + alignment slack
+  l.k = kTcTiles * q_tile_bytes(D);
+  l.v = l.k + kTcKStages * kv_stage_bytes(D);
+  l.bars = l.v + kTcVStages * kv_stage_bytes(D);
+  const int used = l.bars + 32 * 8 + 1024;   // barriers + slot, + alignment slack
+  l.total = used > kMinSmem ? used : kMinSmem;
   return l;
-}
-
-// Shared-memory offset of K/V stage st: two stages after Q, the third in
-// Q's own space (free once Q has been copied into TMEM; same size as a stage).
-__host__ __device__ constexpr int stage_offset(const TcLayout& l, int st, int stage_bytes) {
-  return st < 2 ? l.kv + st * stage_bytes : l.q;
 }
 
 // mbarrier slots
 constexpr int kQFull = 0;
-constexpr int kKvFull = 1;                   // [kTcStages]
-constexpr int kKvEmpty = kKvFull + kTcStages;
-constexpr int kSFull = kKvEmpty + kTcStages; // S_j written
-constexpr int kPFull = kSFull + 1;           // P_j written over S_j (one arrival per softmax warp)
-constexpr int kPvDone = kPFull + 1;          // P_j V_j done: S free for S_{j+1}
-constexpr int kDrain = kPvDone + 1;
-constexpr int kQTmem = kDrain + 1;           // Q copied into TMEM (one arrival per softmax warp)
-constexpr int kSlot = kQTmem + 1;            // TMEM address (4 bytes) after the barriers
+constexpr int kKFull = 1;                       // [kTcKStages]
+constexpr int kKEmpty = kKFull + kTcKStages;    // [kTcKStages]: both S = Q K^T of the stage done
+constexpr int kVFull = kKEmpty + kTcKStages;    // [kTcVStages]
+constexpr int kVEmpty = kVFull + kTcVStages;    // [kTcVStages]: both P V of the stage done
+constexpr int kSFull = kVEmpty + kTcVStages;    // [kTcTiles]: S_t(j) written
+constexpr int kPFull = kSFull + kTcTiles;     // [kTcTiles]: P_t(j) written (one arrival per softmax warp)
+constexpr int kPvDone = kPFull + kTcTiles;    // [kTcTiles]: P_t(j) V_j done
+constexpr int kDrain = kPvDone + kTcTiles;
+constexpr int kSlot = kDrain + 1;             // TMEM address (4 bytes) after the barriers
 
 // 32 consecutive outputs of a row: fp32 accumulators times `inv`.
 __device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], float inv) {
@@ -115,8 +119,9 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   }
 }
 
-// Find (sequence, first query token) of tile `tile_id` from query_start: a
-// warp scan over the sequences' tile counts, the same answer in every warp.
+// Find (sequence, first query token) of work item `tile_id` (QT query tokens
+// each) from query_start: a warp scan over the sequences' item counts, the
+// same answer in every warp.
 template <int QT>
 __device__ __forceinline__ void find_tile(const PrefillParams& p, int tile_id, int lane, int& b, int& i0) {
   b = -1;
@@ -148,19 +153,22 @@ __device__ __forceinline__ void find_tile(const PrefillParams& p, int tile_id, i
 }
 
 template <int D, int G, typename OutT>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-  constexpr int QT = kTcRows / G;            // query tokens per CTA
+  constexpr int QT = kTcRows / G;            // query tokens per tile
+  constexpr int QT2 = kTcTiles * QT;         // per CTA
   constexpr int BOXES = D / 64;
-  constexpr int KSTEPS = D / 16;
+  constexpr int KSTEPS = D / 16;             // K steps of S = Q K^T
+  constexpr int PSTEPS = kTcKv / 16;         // K steps of O += P V
   constexpr TcLayout lay = tc_layout(D);
-  constexpr int KV_HALF = BOXES * kTcKv * 128;   // K (or V) part of a stage
+  constexpr int QTILE = q_tile_bytes(D);
+  constexpr int STAGE = kv_stage_bytes(D);   // 128 tokens of K (or V)
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kTcRows, kTcKv, false);
   constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kTcRows, D, true);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
-  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later (longer) tiles first
+  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later (longer) work first
 
   // query_start must start at 0, never decrease and end within the T rows
   if (blockIdx.x == 0 && g == 0 && warp == 0) {
@@ -173,8 +181,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
 
   int b, i0;
-  find_tile<QT>(p, tile_id, lane, b, i0);
-  if (b < 0) return;  // past the last tile
+  find_tile<QT2>(p, tile_id, lane, b, i0);
+  if (b < 0) return;  // past the last work item
 
   const int q0 = __ldg(p.query_start + b);
   const int n = __ldg(p.query_start + b + 1) - q0;
@@ -183,8 +191,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (threadIdx.x == 0) record_error(p.err, (L < 0 || L > p.MB * kBlockSize) ? kDevErrLength : kDevErrQuery);
     return;
   }
-  const int pos0 = L - n + i0;                     // position of the tile's first query token
-  const int p_max = pos0 + min(QT, n - i0) - 1;    // of its last (<= L - 1)
+  const int pos0 = L - n + i0;                     // position of the CTA's first query token
+  const int p_max = pos0 + min(QT2, n - i0) - 1;   // of its last (<= L - 1)
   const int nkv = p_max / kTcKv + 1;               // stages up to and including p_max
 
   extern __shared__ unsigned char smem_raw[];
@@ -196,18 +204,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(bars + kQFull, 1);
-    for (int i = 0; i < kTcStages; ++i) {
-      mbar_init(bars + kKvFull + i, 1);
-      mbar_init(bars + kKvEmpty + i, 1);
+    for (int i = 0; i < kTcKStages; ++i) {
+      mbar_init(bars + kKFull + i, 1);
+      mbar_init(bars + kKEmpty + i, 1);
     }
-    mbar_init(bars + kSFull, 1);
-    mbar_init(bars + kPFull, 4);   // one arrival per softmax warp
-    mbar_init(bars + kPvDone, 1);
+    for (int i = 0; i < kTcVStages; ++i) {
+      mbar_init(bars + kVFull + i, 1);
+      mbar_init(bars + kVEmpty + i, 1);
+    }
+    for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(bars + kSFull + t, 1);
+      mbar_init(bars + kPFull + t, 4);   // one arrival per softmax warp of the tile
+      mbar_init(bars + kPvDone + t, 1);
+    }
     mbar_init(bars + kDrain, 1);
-    mbar_init(bars + kQTmem, 4);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kTcMmaWarp) {
     tc::tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -216,106 +229,111 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bars + kQFull, BOXES * kTcRows * 128);
+      mbar_arrive_expect_tx(bars + kQFull, kTcTiles * QTILE);
 #pragma unroll
-      for (int c = 0; c < BOXES; ++c)
-        tma_load_3d(sm + lay.q + c * kTcRows * 128, &tmq, c * 64, g * G, q0 + i0, bars + kQFull);
-      const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % kTcStages, use = j / kTcStages;
-        if (use > 0)
-          mbar_wait(bars + kKvEmpty + st, (use - 1) & 1, p.err);  // stage released by P V
-        else if (st == 2)
-          mbar_wait(bars + kQTmem, 0, p.err);  // Q's space: free once Q is in TMEM
-        unsigned char* kst = sm + stage_offset(lay, st, 2 * KV_HALF);
-        int pb[4];
-        uint32_t bytes = 0;
+      for (int t = 0; t < kTcTiles; ++t)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int jb = 4 * j + u;
-          pb[u] = -1;
-          if (jb * kBlockSize <= p_max) {
-            const int e = __ldg(row + jb);
-            if (static_cast<unsigned>(e) < static_cast<unsigned>(p.NB)) {
-              pb[u] = e;
-              bytes += 2 * BOXES * kBlockSize * 128;
-            } else {
-              record_error(p.err, kDevErrBlockId);
-            }
-          }
-        }
-        if (bytes) {
-          mbar_arrive_expect_tx(bars + kKvFull + st, bytes);
+        for (int c = 0; c < BOXES; ++c)
+          tma_load_3d(sm + lay.q + t * QTILE + c * kTcRows * 128, &tmq, c * 64, g * G, q0 + i0 + t * QT,
+                      bars + kQFull);
+    }
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
+    constexpr int BPS = kTcKv / kBlockSize;  // blocks per stage (8)
+    // One half (K or V) of stage j: wait for its ring slot, then one TMA box
+    // per block and 64 dims (blocks past p_max's block are not loaded).
+    auto load_half = [&](int j, bool is_v) {
+      const int jb = BPS * j + lane;
+      const bool used = lane < BPS && jb * kBlockSize <= p_max;
+      int e = used ? __ldg(row + jb) : -1;
+      const bool bad = used && static_cast<unsigned>(e) >= static_cast<unsigned>(p.NB);
+      if (bad) e = -1;
+      if (__any_sync(kFullMask, bad) && lane == 0 && !is_v) record_error(p.err, kDevErrBlockId);
+      const int nvalid = __popc(__ballot_sync(kFullMask, e >= 0));
+      const int depth = is_v ? kTcVStages : kTcKStages;
+      const int st = j % depth, use = j / depth;
+      uint64_t* full = bars + (is_v ? kVFull : kKFull) + st;
+      uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty) + st;
+      unsigned char* dst = sm + (is_v ? lay.v : lay.k) + st * STAGE;
+      if (lane == 0) {
+        if (use > 0) mbar_wait(empty, (use - 1) & 1, p.err);  // slot released by the MMAs that read it
+        if (nvalid > 0)
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(nvalid) * BOXES * kBlockSize * 128);
+        else
+          mbar_arrive(full);  // nothing to copy (a bad id is recorded above)
+      }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (pb[u] < 0) continue;
+      for (int u = 0; u < BPS; ++u) {
+        const int pb = __shfl_sync(kFullMask, e, u);
+        if (lane == 0 && pb >= 0) {
 #pragma unroll
-            for (int c = 0; c < BOXES; ++c) {
-              const int off = c * kTcKv * 128 + u * kBlockSize * 128;
-              tma_load_4d(kst + off, &tmk, c * 64, 0, g, pb[u], bars + kKvFull + st);
-              tma_load_4d(kst + KV_HALF + off, &tmv, c * 64, 0, g, pb[u], bars + kKvFull + st);
-            }
-          }
-        } else {
-          mbar_arrive(bars + kKvFull + st);  // nothing to copy (a bad id is recorded above)
+          for (int c = 0; c < BOXES; ++c)
+            tma_load_4d(dst + c * kTcKv * 128 + u * kBlockSize * 128, is_v ? &tmv : &tmk, c * 64, 0, g, pb, full);
         }
       }
+    };
+    // K runs one stage ahead of V: K(0), then K(j+1) before V(j)
+    load_half(0, false);
+    for (int j = 0; j < nkv; ++j) {
+      if (j + 1 < nkv) load_half(j + 1, false);
+      load_half(j, true);
     }
-  } else if (warp == 5) {
+  } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    // Issue each MMA group as soon as its inputs are ready, whichever comes
-    // first: S_j = Q K_j^T needs stage j loaded and S buffer j % 2 free
-    // (P_{j-2} V done); O += P_j V_j needs P_j written.  Waiting for one
-    // would hold back the other and stall the ring.
+    // Pipe order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1): while tile t's
+    // softmax turns S_t(j+1) into weights, the other tile's MMAs run.
     if (lane == 0) {
-      mbar_wait(bars + kQTmem, 0, p.err);
-      tc::fence_after_sync();
-      int next_qk = 0, next_pv = 0;
-      uint64_t last = global_timer_ns();
-      while (next_pv < nkv) {
-        bool progressed = false;
-        if (next_qk < nkv && next_qk == next_pv) {  // one S buffer: P_{j-1} V_{j-1} issued first
-          const int j = next_qk, st = j % kTcStages;
-          if (mbar_try_wait(bars + kKvFull + st, (j / kTcStages) & 1) &&
-              (j < 1 || mbar_try_wait(bars + kPvDone, (j - 1) & 1))) {
-            tc::fence_after_sync();
-            const uint32_t kst = sm_s + stage_offset(lay, st, 2 * KV_HALF);
+      auto issue_qk = [&](int t, int j) {
+        const uint32_t kst = sm_s + lay.k + (j % kTcKStages) * STAGE;
+        const uint32_t qt = sm_s + lay.q + t * QTILE;
 #pragma unroll
-            for (int k = 0; k < KSTEPS; ++k) {
-              const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
-              tc::mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * k, bd, IDESC_S, k > 0);
-            }
-            tc::commit(smem_addr(bars + kSFull));
-            ++next_qk;
-            progressed = true;
-          }
+        for (int k = 0; k < KSTEPS; ++k) {
+          // box of 64 dims, then the 16-dim step inside its 128-byte rows
+          const uint64_t ad = tc::smem_desc_sw128(qt + (k >> 2) * kTcRows * 128 + (k & 3) * 32, 0, 1024);
+          const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
+          tc::mma_bf16_ss(tmem + kColS + kTcRows * t, ad, bd, IDESC_S, k > 0);
         }
-        if (next_pv < next_qk) {
-          const int jp = next_pv, stp = jp % kTcStages;
-          if (mbar_try_wait(bars + kPFull, jp & 1)) {
-            tc::fence_after_sync();
-            const uint32_t vst = sm_s + stage_offset(lay, stp, 2 * KV_HALF) + KV_HALF;
-            const uint32_t phi = tmem + kColS, plo = phi + kTcKv / 2;  // P over S in TMEM
+        tc::commit(smem_addr(bars + kSFull + t));
+        if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kKEmpty + j % kTcKStages));  // both S of stage j issued
+      };
+      bool ok = mbar_wait(bars + kQFull, 0, p.err);
+      if (ok) ok = mbar_wait(bars + kKFull + 0, 0, p.err);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int sv = j % kTcVStages;
+        const uint32_t vst = sm_s + lay.v + sv * STAGE;
+        for (int t = 0; ok && t < kTcTiles; ++t) {
+          ok = mbar_wait(bars + kPFull + t, j & 1, p.err);
+          if (ok && t == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
+          // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on
+          const uint32_t pcol = tmem + kColS + kTcRows * t;
 #pragma unroll
-            for (int kk = 0; kk < kTcKv / 16; ++kk) {
-              const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
-              tc::mma_bf16_ts(tmem + kColO, phi + 8 * kk, bd, IDESC_O, jp > 0 || kk > 0);
-              tc::mma_bf16_ts(tmem + kColO, plo + 8 * kk, bd, IDESC_O, true);
-            }
-            tc::commit(smem_addr(bars + kPvDone));
-            tc::commit(smem_addr(bars + kKvEmpty + stp));
-            ++next_pv;
-            progressed = true;
+          for (int kk = 0; kk < PSTEPS; ++kk) {
+            const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
+            tc::mma_bf16_ts(tmem + kColO + kTcRows * t, phi, bd, IDESC_O, j > 0 || kk > 0);
+            tc::mma_bf16_ts(tmem + kColO + kTcRows * t, phi + 16, bd, IDESC_O, true);
           }
-        }
-        if (progressed) {
-          last = global_timer_ns();
-        } else if (global_timer_ns() - last > kWaitLimitNs) {
-          record_error(p.err, kDevErrTimeout);
-          break;
+          tc::commit(smem_addr(bars + kPvDone + t));
+          if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kVEmpty + sv));  // both P V of stage j issued
+          if (j + 1 < nkv) {
+            if (t == 0) ok = mbar_wait(bars + kKFull + (j + 1) % kTcKStages, ((j + 1) / kTcKStages) & 1, p.err);
+            // S_t is rewritten only after the P_t V that reads it has completed
+            if (ok) ok = mbar_wait(bars + kPvDone + t, j & 1, p.err);
+            if (ok) {
+              tc::fence_after_sync();
+              issue_qk(t, j + 1);
+            }
+          }
         }
       }
       // every MMA of this thread done before TMEM is freed, whatever happened above
@@ -324,64 +342,46 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
   } else {
     // ---------------------------------------------------------- softmax rows
-    const int r = threadIdx.x;                     // this thread's row (TMEM lane)
-    const int tok = r / G, head = g * G + r % G;
+    const int t = warp / 4;                        // this warpgroup's tile
+    const int r = threadIdx.x - 128 * t;           // this thread's row (TMEM lane)
+    const int tok = t * QT + r / G, head = g * G + r % G;
     const bool ok = i0 + tok < n;
     const int lim = ok ? pos0 + tok : p_max;       // causal limit of the row
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const uint32_t scol = kColS + kTcRows * t, ocol = kColO + kTcRows * t;
     const float scale = p.qk_scale_log2;
-    // This row of Q into TMEM (the A operand of QK^T): from the TMA tile in
-    // shared memory (128-byte rows, 16-byte chunks swizzled by row % 8), 32
-    // columns of two bf16 per box of 64 dims
-    mbar_wait(bars + kQFull, 0, p.err);
-#pragma unroll
-    for (int c = 0; c < BOXES; ++c) {
-      uint32_t v[32];
-      const unsigned char* qrow = sm + lay.q + c * kTcRows * 128 + r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 w = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) * 16));
-        v[4 * ch] = w.x;
-        v[4 * ch + 1] = w.y;
-        v[4 * ch + 2] = w.z;
-        v[4 * ch + 3] = w.w;
-      }
-      tc::st_32x32b_x32(trow + kColQ + 32 * c, v);
-    }
-    tc::wait_st();
-    tc::fence_before_sync();
-    fence_proxy_async_smem();  // the Q reads above before the TMA engine refills this space
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + kQTmem);
     float m_used = -INFINITY, l = 0.f;             // max the weights are taken against; row sum
     for (int j = 0; j < nkv; ++j) {
-      mbar_wait(bars + kSFull, j & 1, p.err);
+      mbar_wait(bars + kSFull + t, j & 1, p.err);
       tc::fence_after_sync();
-      float s[kTcKv];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(trow + kColS + 32 * h, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) s[32 * h + c] = __uint_as_float(v[c]);
-      }
-
       const int t0 = j * kTcKv;
-      if (t0 + kTcKv - 1 > lim) {  // the tile reaches past this row's position
+      // Stages that reach past a row's position take the masked path, for
+      // the whole warp (one path per warp, not one per row)
+      const bool masked = __any_sync(kFullMask, t0 + kTcKv - 1 > lim);
+      // pass 1: the row's maximum over the stage, 64 columns per TMEM load
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+      for (int h2 = 0; h2 < kTcKv / 64; ++h2) {
+        uint32_t v[64];
+        tc::ld_32x32b_x32(trow + scol + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tc::ld_32x32b_x32(trow + scol + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tc::wait_ld();
+        if (!masked) {
 #pragma unroll
-        for (int c = 0; c < kTcKv; ++c) s[c] = t0 + c <= lim ? s[c] : -INFINITY;
+          for (int c = 0; c < 64; c += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+          }
+        } else {
+          const int tb = t0 + 64 * h2;
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            mx0 = fmaxf(mx0, tb + c <= lim ? __uint_as_float(v[c]) : -INFINITY);
+            mx1 = fmaxf(mx1, tb + c + 1 <= lim ? __uint_as_float(v[c + 1]) : -INFINITY);
+          }
+        }
       }
-      // the row's maximum as a tree (6 levels, not a chain of 64)
-      float mt[kTcKv / 2];
-#pragma unroll
-      for (int c = 0; c < kTcKv / 2; ++c) mt[c] = fmaxf(s[c], s[c + kTcKv / 2]);
-#pragma unroll
-      for (int w = kTcKv / 4; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int c = 0; c < w; ++c) mt[c] = fmaxf(mt[c], mt[c + w]);
-      }
-      const float mx = mt[0];
+      const float mx = fmaxf(mx0, mx1);
       // every row sees token 0 in the first stage, so m_new is finite
       const float m_new = fmaxf(m_used, mx * scale);
       const bool need = m_new > m_used + kRescaleSlack;
@@ -391,45 +391,65 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         m_used = m_new;
       }
       if (j >= 1 && __any_sync(kFullMask, need)) {
-        // rescale O: every P V so far (the last is tile j-1) must be finished
-        mbar_wait(bars + kPvDone, (j - 1) & 1, p.err);
-        tc::fence_after_sync();
+        // rescale O_t: idle now, since P_t V of stage j-1 completed before
+        // S_t(j) was written
         const float f = need ? alpha : 1.f;
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
           uint32_t v[32];
-          tc::ld_32x32b_x32(trow + kColO + 32 * c4, v);
+          tc::ld_32x32b_x32(trow + ocol + 32 * c4, v);
           tc::wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
-          tc::st_32x32b_x32(trow + kColO + 32 * c4, v);
+          tc::st_32x32b_x32(trow + ocol + 32 * c4, v);
         }
-        tc::wait_st();
       }
-      // P = 2^(scale s - m_used) <= 2^8 over S in TMEM, two weights per
-      // column in columns [0, 32) of the buffer as bf16 high parts and the
-      // low parts in [32, 64); in two halves of 32 weights
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      // pass 2: P = 2^(scale s - m_used) <= 2^8, 32 tokens (one chunk of S_t's
+      // columns) at a time, two per packed fp32 operation.  Chunk h's weights
+      // go over its own 32 columns, which it has just read: bf16 high parts in
+      // [32h, 32h + 16), low parts in [32h + 16, 32h + 32), two per column.
+      const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m_used, -m_used);
+      float2 l2 = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int h = 0; h < kTcKv / 32; ++h) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(trow + scol + 32 * h, v);
+        tc::wait_ld();
         uint32_t hi[16], lo[16];
+        if (!masked) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a = fast_exp2(fmaf(s[32 * h + 2 * e], scale, -m_used));
-          const float c = fast_exp2(fmaf(s[32 * h + 2 * e + 1], scale, -m_used));
-          l += a + c;
-          split_bf16x2(a, c, hi[e], lo[e]);
+          for (int e = 0; e < 16; ++e) {
+            const float2 y = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nm2);
+            const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+            l2 = fadd2(l2, w);
+            split_bf16x2(w.x, w.y, hi[e], lo[e]);
+          }
+        } else {
+          const int tb = t0 + 32 * h;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = tb + 2 * e <= lim ? __uint_as_float(v[2 * e]) : -INFINITY;
+            const float x1 = tb + 2 * e + 1 <= lim ? __uint_as_float(v[2 * e + 1]) : -INFINITY;
+            const float2 y = ffma2(make_float2(x0, x1), sc2, nm2);
+            const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+            l2 = fadd2(l2, w);
+            split_bf16x2(w.x, w.y, hi[e], lo[e]);
+          }
         }
-        tc::st_32x32b_x16(trow + kColS + 16 * h, hi);
-        tc::st_32x32b_x16(trow + kColS + kTcKv / 2 + 16 * h, lo);
+        tc::st_32x32b_x16(trow + scol + 32 * h, hi);
+        tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
       }
+      l += l2.x + l2.y;
       tc::wait_st();
       if (j == nkv - 1) {
-        // V rows from z0 on may hold anything: past the sequence, or not loaded
+        // V rows from z0 on may hold anything: past the sequence, or not
+        // loaded.  Both warpgroups zero them (the same values), each before
+        // its own P_t V may read the stage.
         const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
         const int z0 = min(L - t0, loaded);
         if (z0 < kTcKv) {
-          unsigned char* vst = sm + stage_offset(lay, j % kTcStages, 2 * KV_HALF) + KV_HALF;
-          for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kSoftmaxThreads) {
+          unsigned char* vst = sm + lay.v + (j % kTcVStages) * STAGE;
+          for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kTcRows) {
             const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
             *reinterpret_cast<uint4*>(vst + (rest >> 3) * kTcKv * 128 + vr * 128 + (rest & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
@@ -439,11 +459,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       tc::fence_before_sync();   // P stores in TMEM before the arrival
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kPFull);
+      if (lane == 0) mbar_arrive(bars + kPFull + t);
     }
 
     // ---- O / l for this row, after the last P V
-    mbar_wait(bars + kPvDone, (nkv - 1) & 1, p.err);
+    mbar_wait(bars + kPvDone + t, (nkv - 1) & 1, p.err);
     tc::fence_after_sync();
     const float inv = 1.f / l;
     OutT* dst = reinterpret_cast<OutT*>(p.out) + static_cast<int64_t>(q0 + i0 + tok) * p.o_st +
@@ -451,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
     for (int c4 = 0; c4 < D / 32; ++c4) {
       uint32_t v[32];
-      tc::ld_32x32b_x32(trow + kColO + 32 * c4, v);
+      tc::ld_32x32b_x32(trow + ocol + 32 * c4, v);
       tc::wait_ld();
       if (ok) store_row32(dst + 32 * c4, v, inv);
     }
@@ -459,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kTcMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -468,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 template <int D, int G, typename OutT>
 cudaError_t launch_tc_typed(const PrefillParams& p, const CUtensorMap& tmq, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, cudaStream_t stream) {
-  constexpr int QT = kTcRows / G;
+  constexpr int QT2 = kTcTiles * (kTcRows / G);
   auto kernel = paged_prefill_tc_kernel<D, G, OutT>;
   static std::atomic<int> smem_set[64];  // one record per instantiation
   const int smem = tc_layout(D).total;
@@ -481,9 +501,9 @@ cudaError_t launch_tc_typed(const PrefillParams& p, const CUtensorMap& tmq, cons
     if (e != cudaSuccess) return e;
     smem_set[dev].store(1);
   }
-  const int64_t tiles = (static_cast<int64_t>(p.T) + QT - 1) / QT + p.B;  // >= sum of ceil(n_b / QT)
-  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.Hkv));
+  const int64_t items = (static_cast<int64_t>(p.T) + QT2 - 1) / QT2 + p.B;  // >= sum of ceil(n_b / QT2)
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(items), static_cast<unsigned>(p.Hkv));
   kernel<<<grid, kTcThreads, smem, stream>>>(tmq, tmk, tmv, p);
   return cudaGetLastError();
 }
