@@ -121,7 +121,8 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 
 // Find (sequence, first query token) of work item `tile_id` (QT query tokens
 // each) from query_start: a warp scan over the sequences' item counts, the
-// same answer in every warp.
+// same answer in every warp.  Items are numbered by sequence, then by
+// position in the run.
 template <int QT>
 __device__ __forceinline__ void find_tile(const PrefillParams& p, int tile_id, int lane, int& b, int& i0) {
   b = -1;
@@ -149,6 +150,45 @@ __device__ __forceinline__ void find_tile(const PrefillParams& p, int tile_id, i
       return;
     }
     base += total;
+  }
+}
+
+// The work item at place k of a longest-first order (k = 0 runs first): a
+// work item's cost grows with the context it attends to, so items go by
+// sequence length (longest first, ties by sequence index), and within a
+// sequence from its last item to its first.  Every CTA derives the order
+// from the lengths (O(B^2 / 32) loads per warp, so only for B <= kLptMaxB;
+// larger batches keep the order of find_tile, reversed).
+constexpr int kLptMaxB = 256;
+template <int QT>
+__device__ __forceinline__ void find_tile_lpt(const PrefillParams& p, int k, int lane, int& b, int& i0) {
+  b = -1;
+  i0 = 0;
+  auto items = [&](int s) {
+    const int n = __ldg(p.query_start + s + 1) - __ldg(p.query_start + s);
+    return n > 0 ? (n + QT - 1) / QT : 0;
+  };
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int bb = b0 + lane;
+    int before = 0, nt = 0;
+    if (bb < p.B) {
+      nt = items(bb);
+      const int Lb = __ldg(p.context_lens + bb);
+      // items of every sequence that comes before bb in the order
+      for (int s = 0; s < p.B; ++s) {
+        const int Ls = __ldg(p.context_lens + s);
+        if (Ls > Lb || (Ls == Lb && s < bb)) before += items(s);
+      }
+    }
+    const bool mine = bb < p.B && k >= before && k < before + nt;
+    const unsigned who = __ballot_sync(kFullMask, mine);
+    if (who) {
+      const int src = __ffs(who) - 1;
+      b = b0 + src;
+      const int idx = k - __shfl_sync(kFullMask, before, src);
+      i0 = (__shfl_sync(kFullMask, nt, src) - 1 - idx) * QT;  // the sequence's last item first
+      return;
+    }
   }
 }
 
@@ -181,7 +221,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   int b, i0;
-  find_tile<QT2>(p, tile_id, lane, b, i0);
+  if (p.B <= kLptMaxB)
+    find_tile_lpt<QT2>(p, static_cast<int>(blockIdx.x), lane, b, i0);
+  else
+    find_tile<QT2>(p, tile_id, lane, b, i0);
   if (b < 0) return;  // past the last work item
 
   const int q0 = __ldg(p.query_start + b);
@@ -285,15 +328,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Pipe order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1): while tile t's
     // softmax turns S_t(j+1) into weights, the other tile's MMAs run.
     if (lane == 0) {
+      // One thread issues every MMA, so each issue should be cheap.  The
+      // descriptors are built once: the start address of a shared-memory
+      // operand sits in a descriptor's low 14 bits (address >> 4, all of this
+      // CTA's shared memory fits), so the tile, the ring slot and the K step
+      // are added to the built descriptor as offsets >> 4.
+      const uint64_t dq0 = tc::smem_desc_sw128(sm_s + lay.q, 0, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(sm_s + lay.k, 0, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(sm_s + lay.v, kTcKv * 128, 1024);
       auto issue_qk = [&](int t, int j) {
-        const uint32_t kst = sm_s + lay.k + (j % kTcKStages) * STAGE;
-        const uint32_t qt = sm_s + lay.q + t * QTILE;
+        const uint64_t dq = dq0 + static_cast<uint32_t>((t * QTILE) >> 4);
+        const uint64_t dk = dk0 + static_cast<uint32_t>(((j % kTcKStages) * STAGE) >> 4);
+        const uint32_t ds = tmem + kColS + kTcRows * t;
 #pragma unroll
         for (int k = 0; k < KSTEPS; ++k) {
           // box of 64 dims, then the 16-dim step inside its 128-byte rows
-          const uint64_t ad = tc::smem_desc_sw128(qt + (k >> 2) * kTcRows * 128 + (k & 3) * 32, 0, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(kst + (k >> 2) * kTcKv * 128 + (k & 3) * 32, 0, 1024);
-          tc::mma_bf16_ss(tmem + kColS + kTcRows * t, ad, bd, IDESC_S, k > 0);
+          tc::mma_bf16_ss(ds, dq + (((k >> 2) * kTcRows * 128 + (k & 3) * 32) >> 4),
+                          dk + (((k >> 2) * kTcKv * 128 + (k & 3) * 32) >> 4), IDESC_S, k > 0);
         }
         tc::commit(smem_addr(bars + kSFull + t));
         if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kKEmpty + j % kTcKStages));  // both S of stage j issued
@@ -307,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const int sv = j % kTcVStages;
-        const uint32_t vst = sm_s + lay.v + sv * STAGE;
+        const uint64_t dv = dv0 + static_cast<uint32_t>((sv * STAGE) >> 4);
         for (int t = 0; ok && t < kTcTiles; ++t) {
           ok = mbar_wait(bars + kPFull + t, j & 1, p.err);
           if (ok && t == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
@@ -315,13 +366,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::fence_after_sync();
           // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
           // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on
-          const uint32_t pcol = tmem + kColS + kTcRows * t;
+          const uint32_t pcol = tmem + kColS + kTcRows * t, dout = tmem + kColO + kTcRows * t;
 #pragma unroll
           for (int kk = 0; kk < PSTEPS; ++kk) {
             const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
-            const uint64_t bd = tc::smem_desc_sw128(vst + kk * 16 * 128, kTcKv * 128, 1024);
-            tc::mma_bf16_ts(tmem + kColO + kTcRows * t, phi, bd, IDESC_O, j > 0 || kk > 0);
-            tc::mma_bf16_ts(tmem + kColO + kTcRows * t, phi + 16, bd, IDESC_O, true);
+            const uint64_t bd = dv + ((kk * 16 * 128) >> 4);  // 16 token rows of 128 bytes
+            tc::mma_bf16_ts(dout, phi, bd, IDESC_O, j > 0 || kk > 0);
+            tc::mma_bf16_ts(dout, phi + 16, bd, IDESC_O, true);
           }
           tc::commit(smem_addr(bars + kPvDone + t));
           if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kVEmpty + sv));  // both P V of stage j issued
@@ -358,26 +409,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Stages that reach past a row's position take the masked path, for
       // the whole warp (one path per warp, not one per row)
       const bool masked = __any_sync(kFullMask, t0 + kTcKv - 1 > lim);
-      // pass 1: the row's maximum over the stage, 64 columns per TMEM load
+      // pass 1: the row's maximum over the stage (four loads, one wait)
       float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll 1
-      for (int h2 = 0; h2 < kTcKv / 64; ++h2) {
-        uint32_t v[64];
-        tc::ld_32x32b_x32(trow + scol + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tc::ld_32x32b_x32(trow + scol + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      {
+        uint32_t v[kTcKv];
+#pragma unroll
+        for (int h = 0; h < kTcKv / 32; ++h)
+          tc::ld_32x32b_x32(trow + scol + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * h));
         tc::wait_ld();
         if (!masked) {
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < kTcKv; c += 4) {
             mx0 = fmax3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             mx1 = fmax3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
           }
         } else {
-          const int tb = t0 + 64 * h2;
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            mx0 = fmaxf(mx0, tb + c <= lim ? __uint_as_float(v[c]) : -INFINITY);
-            mx1 = fmaxf(mx1, tb + c + 1 <= lim ? __uint_as_float(v[c + 1]) : -INFINITY);
+          for (int c = 0; c < kTcKv; c += 2) {
+            mx0 = fmaxf(mx0, t0 + c <= lim ? __uint_as_float(v[c]) : -INFINITY);
+            mx1 = fmaxf(mx1, t0 + c + 1 <= lim ? __uint_as_float(v[c + 1]) : -INFINITY);
           }
         }
       }
@@ -411,33 +461,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m_used, -m_used);
       float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int h = 0; h < kTcKv / 32; ++h) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(trow + scol + 32 * h, v);
+      for (int h2 = 0; h2 < kTcKv / 64; ++h2) {  // two chunks of 32 per TMEM wait
+        uint32_t v[64];
+        tc::ld_32x32b_x32(trow + scol + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tc::ld_32x32b_x32(trow + scol + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tc::wait_ld();
-        uint32_t hi[16], lo[16];
-        if (!masked) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 y = ffma2(make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2, nm2);
-            const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-            l2 = fadd2(l2, w);
-            split_bf16x2(w.x, w.y, hi[e], lo[e]);
-          }
-        } else {
-          const int tb = t0 + 32 * h;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = 2 * h2 + hh;
+          uint32_t hi[16], lo[16];
+          if (!masked) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float x0 = tb + 2 * e <= lim ? __uint_as_float(v[2 * e]) : -INFINITY;
-            const float x1 = tb + 2 * e + 1 <= lim ? __uint_as_float(v[2 * e + 1]) : -INFINITY;
-            const float2 y = ffma2(make_float2(x0, x1), sc2, nm2);
-            const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-            l2 = fadd2(l2, w);
-            split_bf16x2(w.x, w.y, hi[e], lo[e]);
+            for (int e = 0; e < 16; ++e) {
+              const float2 y = ffma2(make_float2(__uint_as_float(v[32 * hh + 2 * e]), __uint_as_float(v[32 * hh + 2 * e + 1])),
+                                     sc2, nm2);
+              const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+              l2 = fadd2(l2, w);
+              split_bf16x2(w.x, w.y, hi[e], lo[e]);
+            }
+          } else {
+            const int tb = t0 + 32 * h;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float x0 = tb + 2 * e <= lim ? __uint_as_float(v[32 * hh + 2 * e]) : -INFINITY;
+              const float x1 = tb + 2 * e + 1 <= lim ? __uint_as_float(v[32 * hh + 2 * e + 1]) : -INFINITY;
+              const float2 y = ffma2(make_float2(x0, x1), sc2, nm2);
+              const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+              l2 = fadd2(l2, w);
+              split_bf16x2(w.x, w.y, hi[e], lo[e]);
+            }
           }
+          tc::st_32x32b_x16(trow + scol + 32 * h, hi);
+          tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
         }
-        tc::st_32x32b_x16(trow + scol + 32 * h, hi);
-        tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
       }
       l += l2.x + l2.y;
       tc::wait_st();
