@@ -76,11 +76,14 @@ __global__ void __launch_bounds__(kPfThreads) paged_prefill_kernel(const __grid_
   constexpr int TILE = tile_bytes(D);
   constexpr int STAGE = 4 * TILE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
-  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  // One-dimensional grid, the KV head fastest, later (longer) tiles first:
+  // the order holds across the heads too (CTAs are dispatched by index).
+  const int g = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hkv));
+  const int tile_id = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv)) - 1 -
+                      static_cast<int>(blockIdx.x / static_cast<unsigned>(p.Hkv));
 
   // query_start must start at 0, never decrease and end within the T rows
-  if (blockIdx.x == 0 && g == 0 && warp == 0) {
+  if (blockIdx.x == 0 && warp == 0) {
     bool bad = lane == 0 && __ldg(p.query_start) != 0;
     for (int b = lane; b < p.B; b += 32) {
       const int s0 = __ldg(p.query_start + b), s1 = __ldg(p.query_start + b + 1);
@@ -376,8 +379,8 @@ cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& tmk,
   if (e != cudaSuccess) return e;
   // sum over sequences of ceil(n_b / QT) <= T / QT + B tiles
   const int64_t tiles = (static_cast<int64_t>(p.T) + QT - 1) / QT + p.B;
-  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.Hkv));
+  if (tiles * p.Hkv > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(tiles * p.Hkv));
   kernel<<<grid, kPfThreads, smem, stream>>>(tmk, tmv, p);
   return cudaGetLastError();
 }

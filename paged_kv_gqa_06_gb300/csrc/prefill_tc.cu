@@ -207,11 +207,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kTcRows, kTcKv, false);
   constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kTcRows, D, true);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
-  const int tile_id = static_cast<int>(gridDim.x - 1 - blockIdx.x);  // later (longer) work first
+  // One-dimensional grid, the KV head fastest: CTA k runs work item k / Hkv
+  // of the longest-first order for KV head k % Hkv, so the order holds
+  // across the heads too (the hardware dispatches CTAs by increasing index).
+  const int g = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hkv));
+  const int item = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.Hkv));
+  const int tile_id = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv)) - 1 - item;  // later (longer) work first
 
   // query_start must start at 0, never decrease and end within the T rows
-  if (blockIdx.x == 0 && g == 0 && warp == 0) {
+  if (blockIdx.x == 0 && warp == 0) {
     bool bad = lane == 0 && __ldg(p.query_start) != 0;
     for (int b = lane; b < p.B; b += 32) {
       const int s0 = __ldg(p.query_start + b), s1 = __ldg(p.query_start + b + 1);
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   int b, i0;
   if (p.B <= kLptMaxB)
-    find_tile_lpt<QT2>(p, static_cast<int>(blockIdx.x), lane, b, i0);
+    find_tile_lpt<QT2>(p, item, lane, b, i0);
   else
     find_tile<QT2>(p, tile_id, lane, b, i0);
   if (b < 0) return;  // past the last work item
@@ -499,11 +503,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::wait_st();
       if (j == nkv - 1) {
         // V rows from z0 on may hold anything: past the sequence, or not
-        // loaded.  Both warpgroups zero them (the same values), each before
-        // its own P_t V may read the stage.
+        // loaded.  Once the stage's copies have landed (a copy that landed
+        // later would overwrite the zeros with the block's tail), both
+        // warpgroups zero them (the same values), each before its own P_t V
+        // may read the stage.
         const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
         const int z0 = min(L - t0, loaded);
         if (z0 < kTcKv) {
+          mbar_wait(bars + kVFull + j % kTcVStages, (j / kTcVStages) & 1, p.err);
           unsigned char* vst = sm + lay.v + (j % kTcVStages) * STAGE;
           for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kTcRows) {
             const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
@@ -558,8 +565,8 @@ cudaError_t launch_tc_typed(const PrefillParams& p, const CUtensorMap& tmq, cons
     smem_set[dev].store(1);
   }
   const int64_t items = (static_cast<int64_t>(p.T) + QT2 - 1) / QT2 + p.B;  // >= sum of ceil(n_b / QT2)
-  if (items > 0x7fffffff) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(items), static_cast<unsigned>(p.Hkv));
+  if (items * p.Hkv > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(items * p.Hkv));
   kernel<<<grid, kTcThreads, smem, stream>>>(tmq, tmk, tmv, p);
   return cudaGetLastError();
 }
