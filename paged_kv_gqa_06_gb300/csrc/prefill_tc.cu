@@ -330,71 +330,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     // Pipe order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1): while tile t's
-    // softmax turns S_t(j+1) into weights, the other tile's MMAs run.
-    if (lane == 0) {
-      // One thread issues every MMA, so each issue should be cheap.  The
-      // descriptors are built once: the start address of a shared-memory
-      // operand sits in a descriptor's low 14 bits (address >> 4, all of this
-      // CTA's shared memory fits), so the tile, the ring slot and the K step
-      // are added to the built descriptor as offsets >> 4.
-      const uint64_t dq0 = tc::smem_desc_sw128(sm_s + lay.q, 0, 1024);
-      const uint64_t dk0 = tc::smem_desc_sw128(sm_s + lay.k, 0, 1024);
-      const uint64_t dv0 = tc::smem_desc_sw128(sm_s + lay.v, kTcKv * 128, 1024);
-      auto issue_qk = [&](int t, int j) {
-        const uint64_t dq = dq0 + static_cast<uint32_t>((t * QTILE) >> 4);
-        const uint64_t dk = dk0 + static_cast<uint32_t>(((j % kTcKStages) * STAGE) >> 4);
-        const uint32_t ds = tmem + kColS + kTcRows * t;
+    // softmax turns S_t(j+1) into weights, the other tile's MMAs run.  The
+    // whole warp runs the loop and its waits, converged; lane 0's instance of
+    // each MMA and commit runs (a predicate inside the instruction), so one
+    // thread issues them all and each commit tracks all of them.  (Issued
+    // under a lane-0 branch, beside the softmax warps, the MMAs took ~84
+    // cycles each, against the 64 one runs.)
+    // The descriptors are built once: the start address of a shared-memory
+    // operand sits in a descriptor's low 14 bits (address >> 4, all of this
+    // CTA's shared memory fits), so the tile, the ring slot and the K step
+    // are added to the built descriptor as offsets >> 4.
+    const uint64_t dq0 = tc::smem_desc_sw128(sm_s + lay.q, 0, 1024);
+    const uint64_t dk0 = tc::smem_desc_sw128(sm_s + lay.k, 0, 1024);
+    const uint64_t dv0 = tc::smem_desc_sw128(sm_s + lay.v, kTcKv * 128, 1024);
+    auto issue_qk = [&](int t, int j) {
+      const uint64_t dq = dq0 + static_cast<uint32_t>((t * QTILE) >> 4);
+      const uint64_t dk = dk0 + static_cast<uint32_t>(((j % kTcKStages) * STAGE) >> 4);
+      const uint32_t ds = tmem + kColS + kTcRows * t;
 #pragma unroll
-        for (int k = 0; k < KSTEPS; ++k) {
-          // box of 64 dims, then the 16-dim step inside its 128-byte rows
-          tc::mma_bf16_ss(ds, dq + (((k >> 2) * kTcRows * 128 + (k & 3) * 32) >> 4),
-                          dk + (((k >> 2) * kTcKv * 128 + (k & 3) * 32) >> 4), IDESC_S, k > 0);
-        }
-        tc::commit(smem_addr(bars + kSFull + t));
-        if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kKEmpty + j % kTcKStages));  // both S of stage j issued
-      };
-      bool ok = mbar_wait(bars + kQFull, 0, p.err);
-      if (ok) ok = mbar_wait(bars + kKFull + 0, 0, p.err);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_qk(0, 0);
-        issue_qk(1, 0);
+      for (int k = 0; k < KSTEPS; ++k) {
+        // box of 64 dims, then the 16-dim step inside its 128-byte rows
+        tc::mma_bf16_ss_lane0(ds, dq + (((k >> 2) * kTcRows * 128 + (k & 3) * 32) >> 4),
+                              dk + (((k >> 2) * kTcKv * 128 + (k & 3) * 32) >> 4), IDESC_S, k > 0);
       }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int sv = j % kTcVStages;
-        const uint64_t dv = dv0 + static_cast<uint32_t>((sv * STAGE) >> 4);
-        for (int t = 0; ok && t < kTcTiles; ++t) {
-          ok = mbar_wait(bars + kPFull + t, j & 1, p.err);
-          if (ok && t == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
-          if (!ok) break;
-          tc::fence_after_sync();
-          // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
-          // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on
-          const uint32_t pcol = tmem + kColS + kTcRows * t, dout = tmem + kColO + kTcRows * t;
-#pragma unroll
-          for (int kk = 0; kk < PSTEPS; ++kk) {
-            const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
-            const uint64_t bd = dv + ((kk * 16 * 128) >> 4);  // 16 token rows of 128 bytes
-            tc::mma_bf16_ts(dout, phi, bd, IDESC_O, j > 0 || kk > 0);
-            tc::mma_bf16_ts(dout, phi + 16, bd, IDESC_O, true);
-          }
-          tc::commit(smem_addr(bars + kPvDone + t));
-          if (t == kTcTiles - 1) tc::commit(smem_addr(bars + kVEmpty + sv));  // both P V of stage j issued
-          if (j + 1 < nkv) {
-            if (t == 0) ok = mbar_wait(bars + kKFull + (j + 1) % kTcKStages, ((j + 1) / kTcKStages) & 1, p.err);
-            // S_t is rewritten only after the P_t V that reads it has completed
-            if (ok) ok = mbar_wait(bars + kPvDone + t, j & 1, p.err);
-            if (ok) {
-              tc::fence_after_sync();
-              issue_qk(t, j + 1);
-            }
-          }
-        }
-      }
-      // every MMA of this thread done before TMEM is freed, whatever happened above
-      tc::commit(smem_addr(bars + kDrain));
-      mbar_wait(bars + kDrain, 0, p.err);
+      tc::commit_lane0(smem_addr(bars + kSFull + t));
+      if (t == kTcTiles - 1) tc::commit_lane0(smem_addr(bars + kKEmpty + j % kTcKStages));  // both S of stage j issued
+    };
+    bool ok = mbar_wait(bars + kQFull, 0, p.err);
+    if (ok) ok = mbar_wait(bars + kKFull + 0, 0, p.err);
+    ok = __all_sync(kFullMask, ok);
+    if (ok) {
+      tc::fence_after_sync();
+      issue_qk(0, 0);
+      issue_qk(1, 0);
     }
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int sv = j % kTcVStages;
+      const uint64_t dv = dv0 + static_cast<uint32_t>((sv * STAGE) >> 4);
+      for (int t = 0; ok && t < kTcTiles; ++t) {
+        ok = mbar_wait(bars + kPFull + t, j & 1, p.err);
+        if (ok && t == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
+        ok = __all_sync(kFullMask, ok);
+        if (!ok) break;
+        tc::fence_after_sync();
+        // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
+        // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on
+        const uint32_t pcol = tmem + kColS + kTcRows * t, dout = tmem + kColO + kTcRows * t;
+#pragma unroll
+        for (int kk = 0; kk < PSTEPS; ++kk) {
+          const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
+          const uint64_t bd = dv + ((kk * 16 * 128) >> 4);  // 16 token rows of 128 bytes
+          tc::mma_bf16_ts_lane0(dout, phi, bd, IDESC_O, j > 0 || kk > 0);
+          tc::mma_bf16_ts_lane0(dout, phi + 16, bd, IDESC_O, true);
+        }
+        tc::commit_lane0(smem_addr(bars + kPvDone + t));
+        if (t == kTcTiles - 1) tc::commit_lane0(smem_addr(bars + kVEmpty + sv));  // both P V of stage j issued
+        if (j + 1 < nkv) {
+          if (t == 0) ok = mbar_wait(bars + kKFull + (j + 1) % kTcKStages, ((j + 1) / kTcKStages) & 1, p.err);
+          // S_t is rewritten only after the P_t V that reads it has completed
+          if (ok) ok = mbar_wait(bars + kPvDone + t, j & 1, p.err);
+          ok = __all_sync(kFullMask, ok);
+          if (ok) {
+            tc::fence_after_sync();
+            issue_qk(t, j + 1);
+          }
+        }
+      }
+    }
+    // every MMA of this warp done before TMEM is freed, whatever happened above
+    tc::commit_lane0(smem_addr(bars + kDrain));
+    mbar_wait(bars + kDrain, 0, p.err);
   } else {
     // ---------------------------------------------------------- softmax rows
     const int t = warp / 4;                        // this warpgroup's tile

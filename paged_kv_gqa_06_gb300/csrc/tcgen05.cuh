@@ -98,6 +98,38 @@ __device__ __forceinline__ void commit(uint32_t bar_smem) {
                : "memory");
 }
 
+// ---- the same three, executed by a whole converged warp: only lane 0's
+// instance runs (a predicate inside the instruction, not a branch), so one
+// thread issues every MMA and commit while the warp runs the issue loop and
+// its waits together.
+__device__ __forceinline__ void mma_bf16_ss_lane0(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .u32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_lane0(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                  bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .u32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+__device__ __forceinline__ void commit_lane0(uint32_t bar_smem) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .u32 l;\n\t"
+      "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar_smem)
+      : "memory");
+}
+
 // ---- TMEM -> registers: this warp's 32 lanes, 32 consecutive columns each
 __device__ __forceinline__ void ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
