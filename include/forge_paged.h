@@ -356,10 +356,24 @@ FORGE_API int forge_paged_gqa_decode_noalloc(const forge_tensor *q, const forge_
  *   out           f32 or bf16 [T, Hq, D], strides as q; rows outside every
  *                 sequence's range are left as they are.
  * D in {64, 128}, Hq / Hkv in {1, 2, 4, 8}.  Enqueues one kernel on `stream`
- * and returns without syncing; no allocation, capturable.  A query_start or
- * length that breaks the rules above is recorded as FORGE_DEVERR_QUERY /
- * FORGE_DEVERR_LENGTH and that sequence's rows are not written; a bad block
- * id as FORGE_DEVERR_BLOCK_ID.
+ * and returns without syncing.  A query_start or length that breaks the rules
+ * above is recorded as FORGE_DEVERR_QUERY / FORGE_DEVERR_LENGTH and that
+ * sequence's rows are not written; a bad block id as FORGE_DEVERR_BLOCK_ID.
+ *
+ * Long contexts: when block_tables can address more than 4096 tokens
+ * (MB * 16 > 4096), each piece of work whose context passes 4096 tokens is
+ * split into context chunks of at most 4096 tokens that run in parallel and
+ * are merged in fp32, so that no single fp32 accumulation runs over more than
+ * 4096 tokens (over 8K and more tokens the bf16 output can pass the 1.6e-2
+ * bound in the worst case).  The chunks' partial rows live in the same
+ * library-owned, stream-ordered scratch as the decode's split partials (see
+ * forge_paged_gqa_decode: grown on demand with cudaMallocAsync on `stream`,
+ * FORGE_ERR_WORKSPACE if it must grow while `stream` is being captured;
+ * make one call of the largest shape first).  It is sized for every possible
+ * chunk, T / (256 / G) + B pieces x Hkv x ceil(MB * 16 / 4096) chunks x 256
+ * rows x (D + 2) x 4 bytes, and is capped at 1 GiB by lengthening the chunks.
+ * With block tables of at most 4096 tokens no scratch is used and the call
+ * allocates nothing.  (The FORGE_PREFILL_KERNEL=mma kernel does not split.)
  */
 FORGE_API int forge_paged_prefill(const forge_tensor *q, const forge_tensor *k_cache,
                                   const forge_tensor *v_cache, const forge_tensor *block_tables,

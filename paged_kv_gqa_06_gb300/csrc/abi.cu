@@ -237,6 +237,10 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // ones it used to zero), whatever shapes share the workspace.
 constexpr int64_t kCounterSlots = 65536;
 constexpr size_t kCounterBytes = kCounterSlots * 4;
+// Prefill context chunks: at most this many 128-token stages per fp32
+// accumulation, and at most this much scratch for the chunks' partial rows.
+constexpr int64_t kPrefillChunkStages = 32;
+constexpr size_t kPrefillScratchCap = size_t(1) << 30;
 
 size_t workspace_bytes_for(int64_t B, int64_t Hq, int64_t D, int64_t s_max) {
   if (s_max <= 1) return 0;
@@ -710,6 +714,36 @@ int forge_paged_prefill(const forge_tensor* q, const forge_tensor* k_cache, cons
   } else {
     CUtensorMap tmq;
     FORGE_TRY(encode_q_map(q, static_cast<int>(G), &tmq));
+    // Context chunks: an item's attention over more than kPrefillChunkStages
+    // stages (4096 tokens) is split into chunks merged in fp32, which bounds
+    // the length of each fp32 accumulation (measured on the constructed
+    // worst case of the bf16 output's error, all weights rounding the same
+    // way and |V| in [7, 8): 0.0158 of the 0.016 bound at 4K tokens in one
+    // accumulation, 0.0164 at 16K).  The scratch holds every possible chunk's
+    // partial rows; if that would pass kPrefillScratchCap the chunks grow, and
+    // without counter slots for every (item, KV head) there is no split.
+    void* ws = nullptr;
+    std::unique_lock<std::mutex> hold;  // the stream's scratch, held until the launch is enqueued
+    const int64_t items = forge::prefill_tc_items(T, B, static_cast<int>(G));
+    const int64_t max_stages = (MB * kBlockSize + 127) / 128;
+    int64_t C = kPrefillChunkStages;
+    auto partial_bytes = [&](int64_t chunks) {
+      const int64_t rows = items * Hkv * chunks * forge::kPrefillChunkRows;
+      return round256(static_cast<size_t>(rows) * D * 4) + static_cast<size_t>(rows) * 2 * 4;
+    };
+    while (max_stages > C && kCounterBytes + partial_bytes((max_stages + C - 1) / C) > kPrefillScratchCap) C *= 2;
+    if (max_stages > C && items * Hkv <= kCounterSlots) {
+      const int64_t chunks = (max_stages + C - 1) / C;
+      FORGE_TRY(cached_workspace(dev, static_cast<cudaStream_t>(stream), kCounterBytes + partial_bytes(chunks), &ws,
+                                 &hold));
+      char* base = static_cast<char*>(ws);
+      p.chunk_stages = static_cast<int>(C);
+      p.max_chunks = static_cast<int>(chunks);
+      p.counters = reinterpret_cast<int*>(base);
+      p.ws_o = reinterpret_cast<float*>(base + kCounterBytes);
+      p.ws_ml = reinterpret_cast<float*>(base + kCounterBytes +
+                                         round256(static_cast<size_t>(items * Hkv * chunks * forge::kPrefillChunkRows) * D * 4));
+    }
     e = forge::launch_prefill_tc(p, tmq, tmk, tmv, static_cast<int>(D), static_cast<int>(G),
                                  out->dtype == FORGE_BF16, static_cast<cudaStream_t>(stream));
   }

@@ -94,6 +94,14 @@ struct PrefillParams {
   int B, Hq, Hkv, NB, MB, T;
   float qk_scale_log2;
   int* err;
+  // Context chunks (tcgen05 kernel): a work item whose context spans more
+  // than chunk_stages 128-token stages is split into end-aligned chunks of at
+  // most chunk_stages stages, one CTA each; each writes its rows' partial
+  // (O, m, l) and the last to arrive merges them.  chunk_stages = 0: no split.
+  int chunk_stages, max_chunks;
+  int* counters;               // [items * Hkv] arrival counters, zero between calls
+  float* ws_o;                 // [items * max_chunks][rows][D] fp32 partial O
+  float* ws_ml;                // [items * max_chunks][rows][2] fp32 (m, l)
 };
 
 // Programmatic dependent launch.  The decode and append kernels are
@@ -366,5 +374,11 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_k, co
 // over q [T, Hq, D] with boxes of 64 dims x G heads x (128 / G) tokens.
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                               const CUtensorMap& tmap_v, int D, int G, bool out_bf16, cudaStream_t stream);
+// Its work items (query-tile pairs) for T query tokens over B sequences at
+// group size G, an upper bound on the sequences' own counts; the grid has
+// items * max(1, max_chunks) * Hkv CTAs.
+int64_t prefill_tc_items(int64_t T, int64_t B, int G);
+// The partial rows of one (item, KV head, chunk): two query tiles of 128.
+constexpr int kPrefillChunkRows = 256;
 
 }  // namespace forge

@@ -69,6 +69,7 @@ constexpr int kColS = 256;                   // S_t (and P_t over it) at kColS +
 constexpr float kRescaleSlack = 8.0f;        // log2 units: weights stay <= 2^8
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kMinSmem = 116 * 1024;         // > half an SM's shared memory: one CTA per SM
+static_assert(kTcTiles * kTcRows == kPrefillChunkRows, "partial rows of a chunk");
 
 struct TcLayout {
   int q, k, v, bars, total;
@@ -207,12 +208,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(kTcRows, kTcKv, false);
   constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(kTcRows, D, true);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid, the KV head fastest: CTA k runs work item k / Hkv
-  // of the longest-first order for KV head k % Hkv, so the order holds
+  // One-dimensional grid, the KV head fastest, then the chunk slot: CTA k
+  // runs chunk slot (k / Hkv) % max_chunks of work item k / (Hkv max_chunks)
+  // of the longest-first order, for KV head k % Hkv, so the order holds
   // across the heads too (the hardware dispatches CTAs by increasing index).
+  const int chunk_slots = max(1, p.max_chunks);
   const int g = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hkv));
-  const int item = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.Hkv));
-  const int tile_id = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv)) - 1 - item;  // later (longer) work first
+  const int unit = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.Hkv));
+  const int item = unit / chunk_slots, cslot = unit % chunk_slots;
+  const int items = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv)) / chunk_slots;
+  const int tile_id = items - 1 - item;  // later (longer) work first
 
   // query_start must start at 0, never decrease and end within the T rows
   if (blockIdx.x == 0 && warp == 0) {
@@ -240,7 +245,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int pos0 = L - n + i0;                     // position of the CTA's first query token
   const int p_max = pos0 + min(QT2, n - i0) - 1;   // of its last (<= L - 1)
-  const int nkv = p_max / kTcKv + 1;               // stages up to and including p_max
+  const int nkv_all = p_max / kTcKv + 1;           // the item's stages, up to and including p_max
+  // Context chunks, aligned to the end: chunk nch-1 ends at stage nkv_all-1,
+  // every chunk but chunk 0 holds C stages and chunk 0 the remaining 1..C.
+  // Chunk slot c runs chunk nch-1-c (the full chunks first).  Every chunk's
+  // first stage starts at or before the item's first query position, so
+  // each row sees a token in it and its running maximum is finite from there.
+  const int C = p.chunk_stages;
+  const int nch = C > 0 ? (nkv_all + C - 1) / C : 1;
+  if (cslot >= nch) return;                        // an empty chunk slot
+  const int ch = nch - 1 - cslot;
+  const int rem = nkv_all - (nch - 1) * (C > 0 ? C : 0);
+  const int st0 = ch == 0 ? 0 : rem + (ch - 1) * C;  // this CTA's first stage
+  const int nkv = ch == 0 ? rem : C;                 // and its stage count
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // One half (K or V) of stage j: wait for its ring slot, then one TMA box
     // per block and 64 dims (blocks past p_max's block are not loaded).
     auto load_half = [&](int j, bool is_v) {
-      const int jb = BPS * j + lane;
+      const int jb = BPS * (st0 + j) + lane;  // j: this CTA's stage index
       const bool used = lane < BPS && jb * kBlockSize <= p_max;
       int e = used ? __ldg(row + jb) : -1;
       const bool bad = used && static_cast<unsigned>(e) >= static_cast<unsigned>(p.NB);
@@ -414,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int j = 0; j < nkv; ++j) {
       mbar_wait(bars + kSFull + t, j & 1, p.err);
       tc::fence_after_sync();
-      const int t0 = j * kTcKv;
+      const int t0 = (st0 + j) * kTcKv;            // position of the stage's first token
       // Stages that reach past a row's position take the masked path, for
       // the whole warp (one path per warp, not one per row)
       const bool masked = __any_sync(kFullMask, t0 + kTcKv - 1 > lim);
@@ -533,15 +550,85 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- O / l for this row, after the last P V
     mbar_wait(bars + kPvDone + t, (nkv - 1) & 1, p.err);
     tc::fence_after_sync();
-    const float inv = 1.f / l;
     OutT* dst = reinterpret_cast<OutT*>(p.out) + static_cast<int64_t>(q0 + i0 + tok) * p.o_st +
                 static_cast<int64_t>(head) * p.o_sh;
+    if (nch == 1) {
+      const float inv = 1.f / l;
 #pragma unroll
-    for (int c4 = 0; c4 < D / 32; ++c4) {
-      uint32_t v[32];
-      tc::ld_32x32b_x32(trow + ocol + 32 * c4, v);
-      tc::wait_ld();
-      if (ok) store_row32(dst + 32 * c4, v, inv);
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(trow + ocol + 32 * c4, v);
+        tc::wait_ld();
+        if (ok) store_row32(dst + 32 * c4, v, inv);
+      }
+    } else {
+      // This chunk's partial row: O (against m_used, not divided), m_used
+      // and l.  Partial rows of (item, KV head g) sit at
+      // ((item Hkv + g) max_chunks + chunk) rows + row.
+      const int64_t base = (static_cast<int64_t>(item) * p.Hkv + g) * chunk_slots;
+      const int row = t * kTcRows + r;
+      constexpr int kRows = kTcTiles * kTcRows;
+      float* po = p.ws_o + ((base + ch) * kRows + row) * D;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(trow + ocol + 32 * c4, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<uint4*>(po + 32 * c4 + c) = make_uint4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+      }
+      *reinterpret_cast<float2*>(p.ws_ml + ((base + ch) * kRows + row) * 2) = make_float2(m_used, l);
+      // Arrival, as in the decode's split merge: the barrier orders every
+      // softmax thread's partial stores before thread 0's acquire-release
+      // atomic, whose release half publishes them; in the last chunk to
+      // arrive its acquire half and the barrier order the other chunks'
+      // partials before every thread's reads.
+      int* counter = p.counters + static_cast<int64_t>(item) * p.Hkv + g;
+      volatile int* last_flag = reinterpret_cast<volatile int*>(bars + kSlot) + 1;
+      named_barrier(1, kTcSoftmaxWarps * 32);
+      if (threadIdx.x == 0) {
+        int old;
+        asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+        *last_flag = old == nch - 1 ? 1 : 0;
+      }
+      named_barrier(1, kTcSoftmaxWarps * 32);
+      if (*last_flag) {
+        // merge the row's nch partials: M = max_c m_c, w_c = 2^(m_c - M),
+        // out = sum_c w_c O_c / sum_c w_c l_c (every chunk saw a token of
+        // the row, so every l_c > 0 and m_c is finite)
+        float M = -INFINITY;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(p.ws_ml + ((base + c) * kRows + row) * 2));
+        float den = 0.f;
+        for (int c = 0; c < nch; ++c) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + ((base + c) * kRows + row) * 2));
+          den = fmaf(fast_exp2(ml.x - M), ml.y, den);
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          for (int c = 0; c < nch; ++c) {
+            const float w = fast_exp2(__ldcg(p.ws_ml + ((base + c) * kRows + row) * 2) - M);
+            const float4* src = reinterpret_cast<const float4*>(p.ws_o + ((base + c) * kRows + row) * D + 32 * c4);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 x = __ldcg(src + e);
+              acc[4 * e] = fmaf(w, x.x, acc[4 * e]);
+              acc[4 * e + 1] = fmaf(w, x.y, acc[4 * e + 1]);
+              acc[4 * e + 2] = fmaf(w, x.z, acc[4 * e + 2]);
+              acc[4 * e + 3] = fmaf(w, x.w, acc[4 * e + 3]);
+            }
+          }
+          uint32_t v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(acc[e]);
+          if (ok) store_row32(dst + 32 * c4, v, inv);
+        }
+        if (threadIdx.x == 0) *counter = 0;  // ready for the next call
+      }
     }
   }
 
@@ -556,7 +643,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int D, int G, typename OutT>
 cudaError_t launch_tc_typed(const PrefillParams& p, const CUtensorMap& tmq, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, cudaStream_t stream) {
-  constexpr int QT2 = kTcTiles * (kTcRows / G);
   auto kernel = paged_prefill_tc_kernel<D, G, OutT>;
   static std::atomic<int> smem_set[64];  // one record per instantiation
   const int smem = tc_layout(D).total;
@@ -569,9 +655,10 @@ cudaError_t launch_tc_typed(const PrefillParams& p, const CUtensorMap& tmq, cons
     if (e != cudaSuccess) return e;
     smem_set[dev].store(1);
   }
-  const int64_t items = (static_cast<int64_t>(p.T) + QT2 - 1) / QT2 + p.B;  // >= sum of ceil(n_b / QT2)
-  if (items * p.Hkv > 0x7fffffff) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(items * p.Hkv));
+  const int64_t items = prefill_tc_items(p.T, p.B, G);  // >= sum of ceil(n_b / QT2)
+  const int64_t ctas = items * std::max(1, p.max_chunks) * p.Hkv;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas));
   kernel<<<grid, kTcThreads, smem, stream>>>(tmq, tmk, tmv, p);
   return cudaGetLastError();
 }
@@ -589,6 +676,11 @@ cudaError_t launch_tc_g(const PrefillParams& p, const CUtensorMap& tmq, const CU
 }
 
 }  // namespace
+
+int64_t prefill_tc_items(int64_t T, int64_t B, int G) {
+  const int64_t qt2 = kTcTiles * (kTcRows / G);  // query tokens per work item
+  return (T + qt2 - 1) / qt2 + B;
+}
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmq, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int D, int G, bool out_bf16, cudaStream_t stream) {

@@ -191,3 +191,49 @@ def test_prefill_rounding_stress():
         print(f"prefill rounding stress out={od}: max-abs error {err:.3e}")
         assert err <= TOL[od], f"{od}: {err}"
     assert binding.forge_paged_get_device_error() == 0
+
+
+def test_prefill_long_contexts_split_into_chunks(kernel):
+    """Contexts past 4096 tokens: the tcgen05 kernel splits each work item's
+    attention into context chunks of at most 32 stages, merged in fp32 by the
+    last chunk to finish (items of 5000 and 9000 tokens take 2 and 3 chunks;
+    the short sequence takes one)."""
+    spec = W.custom_spec("pf_chunks", B=3, Hq=32, Hkv=8, D=128, fixed_lens=(5000, 9000, 300), free_frac=0.1,
+                         seed=414, out_dtype="bf16")
+    pw = W.make_prefill(spec, chunk_lens=(64, 200, 300))
+    t = pw.layer(0)
+    _, _, ref = _oracle(pw, t)
+    d = DevicePrefill(pw, t)
+    d.append()
+    for od in ("f32", "bf16"):
+        err = max_abs_err(d.prefill(od), ref)
+        print(f"prefill long contexts kernel={kernel} out={od}: max-abs error {err:.3e}")
+        assert err <= TOL[od], f"{od}: {err}"
+    # a second call on the same stream: the chunk counters were returned to zero
+    err = max_abs_err(d.prefill("bf16"), ref)
+    assert err <= TOL["bf16"]
+    assert binding.forge_paged_get_device_error() == 0
+
+
+@pytest.mark.parametrize("ctx", [8192, 16384])
+def test_prefill_rounding_stress_long_context(kernel, ctx):
+    """The precision worst case (see test_prefill_rounding_stress) at long
+    contexts, where one fp32 accumulation over the whole context would pass the
+    bf16 bound (0.0160 at 8K tokens, 0.0164 at 16K): the tcgen05 kernel's
+    context chunks keep each accumulation to 4096 tokens.  The mma.sync
+    kernel accumulates the whole context and is not held to this case."""
+    if kernel == "mma_sync":
+        pytest.skip("the mma.sync prefill accumulates the whole context in one fp32 sum")
+    spec = W.custom_spec(f"pf_stress_{ctx}", B=1, Hq=32, Hkv=8, D=128, fixed_lens=(ctx,), free_frac=0.1,
+                         seed=415 + ctx, values="rounding_stress")
+    pw = W.make_prefill(spec, chunk_lens=(64,))
+    t = pw.layer(0)
+    _, _, ref = _oracle(pw, t)
+    assert np.abs(ref).min() >= 7.0
+    d = DevicePrefill(pw, t)
+    d.append()
+    for od in ("f32", "bf16"):
+        err = max_abs_err(d.prefill(od), ref)
+        print(f"prefill rounding stress ctx={ctx} out={od}: max-abs error {err:.3e}")
+        assert err <= TOL[od], f"{od}: {err}"
+    assert binding.forge_paged_get_device_error() == 0
