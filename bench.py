@@ -891,7 +891,7 @@ def run_serving(args, wl):
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": 1, "steps": k, "warmup": warm,
         "ms_per_step": round(ms / k, 5), "us_per_layer_step": round(ms / k * 1e3 / L, 2),
         "pct_of_hbm_peak": round(100 * gbs / peak, 1), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
         "config": {"workload": f"{wl.spec.name} under continuous batching: {L} layers, {rows} rows, requests with "
                                f"lognormal prompts (median {wl.spec.median:g}, sigma {wl.spec.sigma:g}) and "
                                f"decode lengths U[{new_min},{new_max}], closed loop of rows + 16 outstanding",
@@ -1001,7 +1001,7 @@ def run_prefill(args, name):
         "metric": "paged prefill: attention TFLOP/s (causal pairs only) and us per call",
         "value": round(tflops_step, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": reps * copies,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
         "config": {"workload": f"{name}: {pw.spec.description}", "batch": pw.B, "query_tokens": pw.T,
                    "context_tokens": int(pw.context_lens.sum()), "attended_pairs": pairs,
                    "flops_rule": "4 * D * Hq per (query token, attended token)",
