@@ -15,18 +15,22 @@
 //   * warp 8 (producer) loads the two Q tiles once (3-D TMA boxes of 64 dims
 //     x G heads x 128/G tokens, which land as 128 K-major rows each) and
 //     streams the sequence's K and V, 128 tokens (8 blocks) per stage,
-//     through the block table into a 3-stage K ring and a 2-stage V ring, up
-//     to the pair's last query position; K runs a stage ahead of V, since
-//     S = Q K^T of a stage comes before its P V;
+//     through the block table into a 2-stage K ring and a 3-stage V ring, up
+//     to the pair's last query position.  K(j) and V(j) are requested as
+//     soon as their slots free; V's slot frees later (after both P V of a
+//     stage, where K's frees after both Q K^T), so V gets the deeper ring.
+//     Block ids are read 32 at a time (four stages), a group ahead;
 //   * warp 9 (MMA) owns all 512 TMEM columns: O_0, O_1 (D columns each at
 //     0 and 128) and S_0, S_1 (128 columns each at 256 and 384).  Its lane 0
 //     issues S_t = Q_t K_j^T (M 128, N 128, K = D; both operands K-major in
 //     shared memory as TMA wrote them) and O_t += P_t V_j (M 128, N = D,
 //     K 128; P from TMEM over S_t, V MN-major as it lies in the stage).  The
 //     order PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1) keeps one tile's MMAs
-//     running while the other tile's softmax works.  S_t is rewritten only
-//     after the P_t V that reads it has completed (tcgen05.commit on
-//     mbarriers tracks completion and frees stages);
+//     running while the other tile's softmax works; each P V runs in two
+//     halves of 64 tokens, the first as soon as the softmax has written
+//     those tokens' weights.  S_t is rewritten only after the P_t V that
+//     reads it has completed (tcgen05.commit on mbarriers tracks completion
+//     and frees stages);
 //   * warps 0-3 and 4-7 are the softmax warpgroups of tiles 0 and 1: one row
 //     per thread, warp w reading TMEM lanes 32 (w % 4) .. +31.  Per stage:
 //     load the row of S, mask by position (only on stages that reach past
@@ -57,8 +61,8 @@ namespace {
 constexpr int kTcRows = 128;                 // MMA M: rows of one query tile
 constexpr int kTcTiles = 2;                  // query tiles per CTA
 constexpr int kTcKv = 128;                   // tokens per K/V stage (MMA N of S, K of P V)
-constexpr int kTcKStages = 3;                // K ring depth: K runs ahead of V
-constexpr int kTcVStages = 2;                // V ring depth
+constexpr int kTcKStages = 2;                // K ring depth
+constexpr int kTcVStages = 3;                // V ring depth
 constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
 constexpr int kTcProducerWarp = kTcSoftmaxWarps;
 constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
@@ -100,7 +104,8 @@ constexpr int kSFull = kVEmpty + kTcVStages;    // [kTcTiles]: S_t(j) written
 constexpr int kPFull = kSFull + kTcTiles;     // [kTcTiles]: P_t(j) written (one arrival per softmax warp)
 constexpr int kPvDone = kPFull + kTcTiles;    // [kTcTiles]: P_t(j) V_j done
 constexpr int kDrain = kPvDone + kTcTiles;
-constexpr int kSlot = kDrain + 1;             // TMEM address (4 bytes) after the barriers
+constexpr int kPHalf = kDrain + 1;            // [kTcTiles]: P_t(j)'s first half written (one arrival per softmax warp)
+constexpr int kSlot = kPHalf + kTcTiles;      // TMEM address (4 bytes) after the barriers
 
 // 32 consecutive outputs of a row: fp32 accumulators times `inv`.
 __device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], float inv) {
@@ -279,6 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(bars + kSFull + t, 1);
       mbar_init(bars + kPFull + t, 4);   // one arrival per softmax warp of the tile
+      mbar_init(bars + kPHalf + t, 4);
       mbar_init(bars + kPvDone + t, 1);
     }
     mbar_init(bars + kDrain, 1);
@@ -306,12 +312,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.bt_sb;
     constexpr int BPS = kTcKv / kBlockSize;  // blocks per stage (8)
-    // One half (K or V) of stage j: wait for its ring slot, then one TMA box
-    // per block and 64 dims (blocks past p_max's block are not loaded).
-    auto load_half = [&](int j, bool is_v) {
+    constexpr int GRP = 32 / BPS;            // stages per warp-wide table read (4)
+    // Block ids of stages GRP q .. GRP q + GRP - 1: lane l holds block l % BPS
+    // of stage GRP q + l / BPS (entries past p_max's block are not read)
+    auto table_group = [&](int q) -> int {
+      const int jb = BPS * (st0 + GRP * q) + lane;
+      return jb * kBlockSize <= p_max ? __ldg(row + jb) : -1;
+    };
+    // One half (K or V) of stage j, its block ids `grp` (the group holding
+    // stage j): wait for its ring slot, then one TMA box per block and 64
+    // dims (blocks past p_max's block are not loaded).
+    auto load_half = [&](int j, bool is_v, int grp) {
       const int jb = BPS * (st0 + j) + lane;  // j: this CTA's stage index
       const bool used = lane < BPS && jb * kBlockSize <= p_max;
-      int e = used ? __ldg(row + jb) : -1;
+      const int eg = __shfl_sync(kFullMask, grp, (j % GRP) * BPS + (lane % BPS));
+      int e = used ? eg : -1;
       const bool bad = used && static_cast<unsigned>(e) >= static_cast<unsigned>(p.NB);
       if (bad) e = -1;
       if (__any_sync(kFullMask, bad) && lane == 0 && !is_v) record_error(p.err, kDevErrBlockId);
@@ -338,11 +353,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     };
-    // K runs one stage ahead of V: K(0), then K(j+1) before V(j)
-    load_half(0, false);
+    // K(j) then V(j): each waits only for its own slot, released by QK^T of
+    // stage j - 2 (K) or P V of stage j - 3 (V).  The block ids are read a
+    // group of stages ahead, so no table read waits in this loop.
+    int cur = table_group(0), nxt = nkv > GRP ? table_group(1) : -1;
     for (int j = 0; j < nkv; ++j) {
-      if (j + 1 < nkv) load_half(j + 1, false);
-      load_half(j, true);
+      if (j > 0 && j % GRP == 0) {
+        cur = nxt;
+        nxt = j + GRP < nkv ? table_group(j / GRP + 1) : -1;
+      }
+      load_half(j, false, cur);
+      load_half(j, true, cur);
     }
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issue
@@ -385,21 +406,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int sv = j % kTcVStages;
       const uint64_t dv = dv0 + static_cast<uint32_t>((sv * STAGE) >> 4);
       for (int t = 0; ok && t < kTcTiles; ++t) {
-        ok = mbar_wait(bars + kPFull + t, j & 1, p.err);
-        if (ok && t == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
-        ok = __all_sync(kFullMask, ok);
-        if (!ok) break;
-        tc::fence_after_sync();
         // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
-        // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on
+        // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on.
+        // The first half of the K steps runs once the softmax has written the
+        // first 64 tokens' weights, while it computes the rest.
         const uint32_t pcol = tmem + kColS + kTcRows * t, dout = tmem + kColO + kTcRows * t;
+        for (int half = 0; ok && half < 2; ++half) {
+          ok = mbar_wait(bars + (half == 0 ? kPHalf : kPFull) + t, j & 1, p.err);
+          if (ok && t == 0 && half == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
+          ok = __all_sync(kFullMask, ok);
+          if (!ok) break;
+          tc::fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < PSTEPS; ++kk) {
-          const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
-          const uint64_t bd = dv + ((kk * 16 * 128) >> 4);  // 16 token rows of 128 bytes
-          tc::mma_bf16_ts_lane0(dout, phi, bd, IDESC_O, j > 0 || kk > 0);
-          tc::mma_bf16_ts_lane0(dout, phi + 16, bd, IDESC_O, true);
+          for (int k2 = 0; k2 < PSTEPS / 2; ++k2) {
+            const int kk = half * (PSTEPS / 2) + k2;
+            const uint32_t phi = pcol + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint64_t bd = dv + ((kk * 16 * 128) >> 4);  // 16 token rows of 128 bytes
+            tc::mma_bf16_ts_lane0(dout, phi, bd, IDESC_O, j > 0 || kk > 0);
+            tc::mma_bf16_ts_lane0(dout, phi + 16, bd, IDESC_O, true);
+          }
         }
+        if (!ok) break;
         tc::commit_lane0(smem_addr(bars + kPvDone + t));
         if (t == kTcTiles - 1) tc::commit_lane0(smem_addr(bars + kVEmpty + sv));  // both P V of stage j issued
         if (j + 1 < nkv) {
@@ -480,6 +507,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::st_32x32b_x32(trow + ocol + 32 * c4, v);
         }
       }
+      if (j == nkv - 1) {
+        // V rows from z0 on may hold anything: past the sequence, or not
+        // loaded.  Once the stage's copies have landed (a copy that landed
+        // later would overwrite the zeros with the block's tail), both
+        // warpgroups zero them (the same values), each before the first
+        // half of its own P_t V may read the stage.
+        const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
+        const int z0 = min(L - t0, loaded);
+        if (z0 < kTcKv) {
+          mbar_wait(bars + kVFull + j % kTcVStages, (j / kTcVStages) & 1, p.err);
+          unsigned char* vst = sm + lay.v + (j % kTcVStages) * STAGE;
+          for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kTcRows) {
+            const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
+            *reinterpret_cast<uint4*>(vst + (rest >> 3) * kTcKv * 128 + vr * 128 + (rest & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
       // pass 2: P = 2^(scale s - m_used) <= 2^8, 32 tokens (one chunk of S_t's
       // columns) at a time, two per packed fp32 operation.  Chunk h's weights
       // go over its own 32 columns, which it has just read: bf16 high parts in
@@ -520,29 +566,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::st_32x32b_x16(trow + scol + 32 * h, hi);
           tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
         }
+        if (h2 == 0) {  // the first 64 tokens' weights: their half of P_t V may start
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + kPHalf + t);
+        }
       }
       l += l2.x + l2.y;
       tc::wait_st();
-      if (j == nkv - 1) {
-        // V rows from z0 on may hold anything: past the sequence, or not
-        // loaded.  Once the stage's copies have landed (a copy that landed
-        // later would overwrite the zeros with the block's tail), both
-        // warpgroups zero them (the same values), each before its own P_t V
-        // may read the stage.
-        const int loaded = min(kTcKv / kBlockSize, (p_max - t0) / kBlockSize + 1) * kBlockSize;
-        const int z0 = min(L - t0, loaded);
-        if (z0 < kTcKv) {
-          mbar_wait(bars + kVFull + j % kTcVStages, (j / kTcVStages) & 1, p.err);
-          unsigned char* vst = sm + lay.v + (j % kTcVStages) * STAGE;
-          for (int idx = r; idx < (kTcKv - z0) * BOXES * 8; idx += kTcRows) {
-            const int vr = z0 + idx / (BOXES * 8), rest = idx % (BOXES * 8);
-            *reinterpret_cast<uint4*>(vst + (rest >> 3) * kTcKv * 128 + vr * 128 + (rest & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-      }
-      fence_proxy_async_smem();  // zeroed V rows visible to the tensor cores
-      tc::fence_before_sync();   // P stores in TMEM before the arrival
+      tc::fence_before_sync();  // P stores in TMEM before the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + kPFull + t);
     }
