@@ -19,7 +19,9 @@
 //     to the pair's last query position.  K(j) and V(j) are requested as
 //     soon as their slots free; V's slot frees later (after both P V of a
 //     stage, where K's frees after both Q K^T), so V gets the deeper ring.
-//     Block ids are read 32 at a time (four stages), a group ahead;
+//     Block ids are read 32 at a time (four stages), a group ahead, and
+//     lane u issues block u's boxes: issued from one thread, a half-stage's
+//     16 boxes took longer than the MMAs that read them;
 //   * warp 9 (MMA) owns all 512 TMEM columns: O_0, O_1 (D columns each at
 //     0 and 128) and S_0, S_1 (128 columns each at 256 and 384).  Its lane 0
 //     issues S_t = Q_t K_j^T (M 128, N 128, K = D; both operands K-major in
@@ -336,21 +338,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint64_t* full = bars + (is_v ? kVFull : kKFull) + st;
       uint64_t* empty = bars + (is_v ? kVEmpty : kKEmpty) + st;
       unsigned char* dst = sm + (is_v ? lay.v : lay.k) + st * STAGE;
+      // the whole warp waits for the slot, released by the MMAs that read it
+      if (use > 0) mbar_wait(empty, (use - 1) & 1, p.err);
       if (lane == 0) {
-        if (use > 0) mbar_wait(empty, (use - 1) & 1, p.err);  // slot released by the MMAs that read it
         if (nvalid > 0)
           mbar_arrive_expect_tx(full, static_cast<uint32_t>(nvalid) * BOXES * kBlockSize * 128);
         else
           mbar_arrive(full);  // nothing to copy (a bad id is recorded above)
       }
+      __syncwarp();
+      // lane u < BPS copies block u: eight issuing threads, not one
+      if (e >= 0) {
 #pragma unroll
-      for (int u = 0; u < BPS; ++u) {
-        const int pb = __shfl_sync(kFullMask, e, u);
-        if (lane == 0 && pb >= 0) {
-#pragma unroll
-          for (int c = 0; c < BOXES; ++c)
-            tma_load_4d(dst + c * kTcKv * 128 + u * kBlockSize * 128, is_v ? &tmv : &tmk, c * 64, 0, g, pb, full);
-        }
+        for (int c = 0; c < BOXES; ++c)
+          tma_load_4d(dst + c * kTcKv * 128 + lane * kBlockSize * 128, is_v ? &tmv : &tmk, c * 64, 0, g, e, full);
       }
     };
     // K(j) then V(j): each waits only for its own slot, released by QK^T of
