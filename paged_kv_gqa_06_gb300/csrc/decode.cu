@@ -542,19 +542,21 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
 #pragma unroll
         for (int u = 0; u < kStageBlocks; ++u)
           if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += TILE_BYTES;
-        if (bytes) {
+        if (bytes)
           mbar_arrive_expect_tx(full + slot, bytes);
-          const CUtensorMap* map = is_v ? &tmv : &tmk;
-#pragma unroll
-          for (int u = 0; u < kStageBlocks; ++u) {
-            if (static_cast<unsigned>(pb[u]) >= static_cast<unsigned>(p.NB)) continue;
-            unsigned char* tile = ring + (slot * kStageBlocks + u) * TILE_BYTES;
-#pragma unroll
-            for (int c = 0; c < BOXES; ++c) tma_load_4d(tile + c * kBoxBytes, map, c * kBoxDims, 0, g, pb[u], full + slot);
-          }
-        } else {
+        else
           mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
-        }
+      }
+      __syncwarp();
+      // one box per lane: lane u * BOXES + c copies box c of block u
+      if (lane < kStageBlocks * BOXES) {
+        const int u = lane / BOXES, c = lane % BOXES;
+        int pbu = pb[0];
+#pragma unroll
+        for (int k = 1; k < kStageBlocks; ++k) pbu = u == k ? pb[k] : pbu;
+        if (static_cast<unsigned>(pbu) < static_cast<unsigned>(p.NB))
+          tma_load_4d(ring + (slot * kStageBlocks + u) * TILE_BYTES + c * kBoxBytes, is_v ? &tmv : &tmk,
+                      c * kBoxDims, 0, g, pbu, full + slot);
       }
       if (++slot == nstage) {
         slot = 0;
@@ -970,22 +972,22 @@ __global__ void __launch_bounds__(kThreads, 5) paged_gqa_decode_online_kernel(co
 #pragma unroll
         for (int u = 0; u < kStageBlocks; ++u)
           if (static_cast<unsigned>(pb[u]) < static_cast<unsigned>(p.NB)) bytes += 2 * TILE_BYTES;
-        if (bytes) {
+        if (bytes)
           mbar_arrive_expect_tx(full + slot, bytes);
-#pragma unroll
-          for (int u = 0; u < kStageBlocks; ++u) {
-            if (static_cast<unsigned>(pb[u]) >= static_cast<unsigned>(p.NB)) continue;
-            unsigned char* kt = ring + (slot * 2 * kStageBlocks + u) * TILE_BYTES;
-            unsigned char* vt = ring + (slot * 2 * kStageBlocks + kStageBlocks + u) * TILE_BYTES;
-#pragma unroll
-            for (int c = 0; c < BOXES; ++c) {
-              tma_load_4d(kt + c * kBoxBytes, &tmk, c * kBoxDims, 0, g, pb[u], full + slot);
-              tma_load_4d(vt + c * kBoxBytes, &tmv, c * kBoxDims, 0, g, pb[u], full + slot);
-            }
-          }
-        } else {
+        else
           mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
-        }
+      }
+      __syncwarp();
+      // one box per lane: lane (u * 2 + kv) * BOXES + c copies box c of block
+      // u's K (kv 0) or V (kv 1)
+      if (lane < kStageBlocks * 2 * BOXES) {
+        const int u = lane / (2 * BOXES), kv = (lane / BOXES) % 2, c = lane % BOXES;
+        int pbu = pb[0];
+#pragma unroll
+        for (int k = 1; k < kStageBlocks; ++k) pbu = u == k ? pb[k] : pbu;
+        if (static_cast<unsigned>(pbu) < static_cast<unsigned>(p.NB))
+          tma_load_4d(ring + (slot * 2 * kStageBlocks + kv * kStageBlocks + u) * TILE_BYTES + c * kBoxBytes,
+                      kv ? &tmv : &tmk, c * kBoxDims, 0, g, pbu, full + slot);
       }
       if (++slot == nstage) {
         slot = 0;
