@@ -139,7 +139,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Tensor map over a [NB, Hkv, 16, D] bf16 cache, dims listed innermost first
 // (D, token, head, block), boxes of 64 dims x 16 tokens (128-byte rows) with
-// the 128-byte swizzle the decode kernel's shared-memory addressing expects.
+// the 128-byte swizzle the kernels' shared-memory addressing expects.
 int encode_cache_map(const forge_tensor* c, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return FORGE_ERR_CUDA;
@@ -154,6 +154,30 @@ int encode_cache_map(const forge_tensor* c, CUtensorMap* map) {
   static unsigned char dummy[16] __attribute__((aligned(16)));
   if (!base) base = dummy;  // empty pool: the map is never used
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_UNSUPPORTED;
+}
+
+// The same cache as a 5-D tensor map whose box is a whole (block, head) tile:
+// dims innermost first (64 dims, token, 64-dim half, head, block), box
+// 64 x 16 x D/64.  It lands as D/64 swizzled 2 KB sub-tiles of 16 rows x
+// 128 bytes, one per half, the layout two boxes of the 4-D map give, in one
+// copy instead of D/64.
+int encode_cache_tile_map(const forge_tensor* c, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return FORGE_ERR_CUDA;
+  const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(kBlockSize), static_cast<cuuint64_t>(c->shape[3] / 64),
+                              static_cast<cuuint64_t>(c->shape[1]),
+                              static_cast<cuuint64_t>(c->shape[0] > 0 ? c->shape[0] : 1)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(c->stride[2]) * 2, 128,
+                                 static_cast<cuuint64_t>(c->stride[1]) * 2, static_cast<cuuint64_t>(c->stride[0]) * 2};
+  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(kBlockSize), static_cast<cuuint32_t>(c->shape[3] / 64), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  void* base = c->data;
+  static unsigned char dummy[16] __attribute__((aligned(16)));
+  if (!base) base = dummy;  // empty pool: the map is never used
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_UNSUPPORTED;
@@ -357,8 +381,8 @@ void attach_workspace(DecodePlan* plan, void* ws) {
 
 int launch_plan(DecodePlan* plan, cudaStream_t stream) {
   CUtensorMap tmk, tmv;
-  FORGE_TRY(encode_cache_map(plan->k_cache, &tmk));
-  FORGE_TRY(encode_cache_map(plan->v_cache, &tmv));
+  FORGE_TRY(encode_cache_tile_map(plan->k_cache, &tmk));
+  FORGE_TRY(encode_cache_tile_map(plan->v_cache, &tmv));
   if (forge::launch_decode(plan->p, tmk, tmv, plan->D, plan->G, plan->out_bf16, stream) != cudaSuccess)
     return FORGE_ERR_CUDA;
   return FORGE_OK;

@@ -230,11 +230,8 @@ __device__ __forceinline__ void prefetch_first_stages(const CUtensorMap* tmk, co
   if (s >= w.nsplit || lane >= min(w.n, stages * 2)) return;
   const int pb = ld_cg(p.block_tables + static_cast<int64_t>(b) * p.bt_sb + w.blk0 + lane);
   if (static_cast<unsigned>(pb) >= static_cast<unsigned>(p.NB)) return;
-#pragma unroll
-  for (int c = 0; c < D / kBoxDims; ++c) {
-    tma_prefetch_4d(tmk, c * kBoxDims, 0, g, pb);
-    tma_prefetch_4d(tmv, c * kBoxDims, 0, g, pb);
-  }
+  tma_prefetch_5d(tmk, 0, 0, 0, g, pb);
+  tma_prefetch_5d(tmv, 0, 0, 0, g, pb);
 }
 
 // Fused append: put this step's new row (`src`, D bf16) into row `r` of the
@@ -548,15 +545,14 @@ __global__ void __launch_bounds__(kThreads, split_min_blocks<G>()) paged_gqa_dec
           mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
       }
       __syncwarp();
-      // one box per lane: lane u * BOXES + c copies box c of block u
-      if (lane < kStageBlocks * BOXES) {
-        const int u = lane / BOXES, c = lane % BOXES;
+      // one (block, head) tile per lane: lane u copies block u
+      if (lane < kStageBlocks) {
         int pbu = pb[0];
 #pragma unroll
-        for (int k = 1; k < kStageBlocks; ++k) pbu = u == k ? pb[k] : pbu;
+        for (int k = 1; k < kStageBlocks; ++k) pbu = lane == k ? pb[k] : pbu;
         if (static_cast<unsigned>(pbu) < static_cast<unsigned>(p.NB))
-          tma_load_4d(ring + (slot * kStageBlocks + u) * TILE_BYTES + c * kBoxBytes, is_v ? &tmv : &tmk,
-                      c * kBoxDims, 0, g, pbu, full + slot);
+          tma_load_5d(ring + (slot * kStageBlocks + lane) * TILE_BYTES, is_v ? &tmv : &tmk, 0, 0, 0, g, pbu,
+                      full + slot);
       }
       if (++slot == nstage) {
         slot = 0;
@@ -978,16 +974,16 @@ __global__ void __launch_bounds__(kThreads, 5) paged_gqa_decode_online_kernel(co
           mbar_arrive(full + slot);  // nothing to copy (bad ids are recorded above)
       }
       __syncwarp();
-      // one box per lane: lane (u * 2 + kv) * BOXES + c copies box c of block
-      // u's K (kv 0) or V (kv 1)
-      if (lane < kStageBlocks * 2 * BOXES) {
-        const int u = lane / (2 * BOXES), kv = (lane / BOXES) % 2, c = lane % BOXES;
+      // one (block, head) tile per lane: lane 2 u + kv copies block u's K
+      // (kv 0) or V (kv 1)
+      if (lane < kStageBlocks * 2) {
+        const int u = lane / 2, kv = lane % 2;
         int pbu = pb[0];
 #pragma unroll
         for (int k = 1; k < kStageBlocks; ++k) pbu = u == k ? pb[k] : pbu;
         if (static_cast<unsigned>(pbu) < static_cast<unsigned>(p.NB))
-          tma_load_4d(ring + (slot * 2 * kStageBlocks + kv * kStageBlocks + u) * TILE_BYTES + c * kBoxBytes,
-                      kv ? &tmv : &tmk, c * kBoxDims, 0, g, pbu, full + slot);
+          tma_load_5d(ring + (slot * 2 * kStageBlocks + kv * kStageBlocks + u) * TILE_BYTES, kv ? &tmv : &tmk, 0, 0,
+                      0, g, pbu, full + slot);
       }
       if (++slot == nstage) {
         slot = 0;
