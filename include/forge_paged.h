@@ -192,10 +192,9 @@ FORGE_API size_t forge_paged_gqa_decode_workspace_bytes(int B, int Hq, int Hkv, 
  * forge_paged_gqa_decode_ex (0 = automatic).  Automatic length: the longest
  * split from 1024 tokens, halving down to 64, whose upper bound on CTAs
  * (B * Hkv * ceil(max_blocks_per_seq * 16 / split)) reaches 4 * num_sms.
- * Kernel: FORGE_DECODE_ONLINE for splits of 512 tokens or more, else
- * FORGE_DECODE_TWO_PASS (an automatic two-pass split is at most 512 tokens);
- * the environment variable FORGE_DECODE_KERNEL ("online" / "two_pass")
- * overrides the kernel.  Writes *split_tokens_out and *kernel_out; returns
+ * Kernel: FORGE_DECODE_ONLINE; the environment variable FORGE_DECODE_KERNEL
+ * ("online" / "two_pass") overrides it (an automatic two-pass split is at
+ * most 512 tokens).  Writes *split_tokens_out and *kernel_out; returns
  * FORGE_OK, FORGE_ERR_NULL, FORGE_ERR_VALUE (bad split_tokens or num_sms) or
  * FORGE_ERR_SHAPE (negative sizes).  Host-only, no CUDA call.
  */

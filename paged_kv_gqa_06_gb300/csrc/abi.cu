@@ -27,7 +27,7 @@ __device__ int g_device_error;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSplitTokens = 512;     // longest automatic split of the two-pass kernel
-constexpr int kOnlineMinSplitTokens = 512;   // automatic kernel choice: single-pass from here up
+constexpr int kOnlineDeepRingTokens = 512;   // single-pass ring: 3 stages on splits from here up, 2 below
 constexpr int kMaxSplitTokens = 1024;  // producer lanes hold <= 64 table entries
 constexpr int kMinSplitTokens = 16;
 
@@ -246,7 +246,7 @@ int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms, int*
     }
   }
   const int forced = decode_kernel_forced();
-  *online = forced ? (forced == 2) : (bps * kBlockSize >= kOnlineMinSplitTokens);
+  *online = forced ? (forced == 2) : 1;  // the two-pass kernel only when FORGE_DECODE_KERNEL asks
   if (split_tokens == 0 && !*online) bps = std::min(bps, kDefaultSplitTokens / kBlockSize);
   return bps;
 }
@@ -273,11 +273,16 @@ size_t workspace_bytes_for(int64_t B, int64_t Hq, int64_t D, int64_t s_max) {
   return kCounterBytes + round256(acc) + ml;
 }
 
-// Ring depth, unless FORGE_PAGED_NSTAGE sets one for both kernels: 3 stages
-// for the single-pass kernel; for the two-pass kernel 3 on splits of up to
-// 256 tokens (its logits buffer is small there, so the third stage costs no
-// occupancy: Qwen3-0.6B-shaped batch of 8, 13.16 against 13.53 us at 128-token
-// splits) and 2 above (Qwen3-4B-shaped batch at 512: 97.9 against 100.5 us).
+// Ring depth, unless FORGE_PAGED_NSTAGE sets one for both kernels.
+// Single-pass kernel: 3 stages on splits of 512 tokens or more (Qwen3-4B-shaped
+// batch at 1024: 94.2 us, against 96.1 and 99.6 at 2 and 4 stages); 2 on
+// shorter splits, which the plan gives only to small problems: the smaller
+// ring lets a fifth CTA onto each SM, so the grid runs in one wave
+// (Qwen3-0.6B-shaped batch of 8 at 128-token splits: 10.97 us, against 13.95
+// at 3 stages and 11.72 for the two-pass kernel).  Two-pass kernel (when
+// forced): 3 on splits of up to 256 tokens (its logits buffer is small there,
+// so the third stage costs no occupancy) and 2 above (Qwen3-4B-shaped batch
+// at 512: 97.9 against 100.5 us).
 int nstage_for(bool online, int bps) {
   static int v = [] {
     const char* e = std::getenv("FORGE_PAGED_NSTAGE");
@@ -285,7 +290,7 @@ int nstage_for(bool online, int bps) {
     return (n >= 2 && n <= 16) ? n : 0;
   }();
   if (v) return v;
-  if (online) return 3;
+  if (online) return bps * kBlockSize >= kOnlineDeepRingTokens ? 3 : 2;
   return bps * kBlockSize <= 256 ? 3 : 2;
 }
 

@@ -15,9 +15,10 @@
 //     `bps` consecutive KV blocks of one sequence;
 //   * warp 2 is the producer: it translates logical blocks through the block
 //     table and streams the split's K tiles, then its V tiles, into a ring of
-//     shared-memory stages with tiled TMA copies (tensor maps over the cache,
-//     128-byte swizzle).  A stage holds two (block, head) tiles of 16 x D
-//     bf16 and is tracked by one mbarrier;
+//     shared-memory stages with tiled TMA copies (5-D tensor maps over the
+//     cache, 128-byte swizzle, one copy per (block, head) tile, issued by the
+//     lane of that tile).  A stage holds two tiles of 16 x D bf16 and is
+//     tracked by one mbarrier;
 //   * warps 0 and 1 consume one tile each per stage on the tensor cores
 //     (mma.sync m16n8k16, bf16 in, fp32 accumulate; the G <= 8 query heads
 //     fill the n = 8 side).  Pass 1: logits S^T = K q^T, 16 tokens per tile,
@@ -35,8 +36,8 @@
 // That is the two-pass kernel.  A second, single-pass kernel on the same grid
 // (further below) carries K and V of the same blocks in each stage and keeps
 // a running maximum and sum instead of a logits buffer, so all of its shared
-// memory is K/V ring.  The host plan (abi.cu) gives splits of 512 tokens or
-// more to the single-pass kernel and shorter ones to the two-pass kernel.
+// memory is K/V ring.  The host plan (abi.cu) runs the single-pass kernel
+// unless FORGE_DECODE_KERNEL selects the two-pass one.
 // Both are launched with programmatic stream serialization.  Before
 // griddepcontrol.wait a CTA only reads its sequence length and block-table
 // entries through L2 to prefetch its first K/V tiles into L2 (the values may

@@ -251,17 +251,17 @@ def test_prefill_empty_is_a_no_op(lib):
 
 
 # (B, Hkv, table width in blocks) of the Qwen3-4B / 36-layer / skewed / Qwen3-0.6B decode
-# workloads, and the plan the policy gives on 152 SMs: 1024-token splits and the
-# single-pass kernel while B * Hkv * ceil(MB * 16 / split) >= 4 * 152, else the
-# longest shorter split that gets there, on the two-pass kernel.
+# workloads, and the plan the policy gives on 152 SMs: 1024-token splits while
+# B * Hkv * ceil(MB * 16 / split) >= 4 * 152, else the longest shorter split that gets
+# there; the single-pass kernel either way.
 @pytest.mark.parametrize("B,Hkv,MB,want", [
     (32, 8, 498, (1024, "online")),      # 256 * 8 = 2048 CTAs at 1024 tokens
     (64, 8, 457, (1024, "online")),      # 512 * 8
     (4, 8, 2048, (1024, "online")),      # 32 * 32 = 1024
-    (8, 8, 116, (128, "two_pass")),      # 64 * 2 < 608, ... 64 * 15 = 960 at 128 tokens
-    (16, 8, 128, (256, "two_pass")),     # 128 * 8 = 1024 at 256 tokens
-    (32, 8, 64, (256, "two_pass")),      # 256 * 2 = 512 < 608 at 512 tokens
-    (0, 8, 10, (64, "two_pass")),        # nothing to run: the shortest split
+    (8, 8, 116, (128, "online")),        # 64 * 2 < 608, ... 64 * 15 = 960 at 128 tokens
+    (16, 8, 128, (256, "online")),       # 128 * 8 = 1024 at 256 tokens
+    (32, 8, 64, (256, "online")),        # 256 * 2 = 512 < 608 at 512 tokens
+    (0, 8, 10, (64, "online")),          # nothing to run: the shortest split
 ])
 def test_decode_plan_policy(lib, monkeypatch, B, Hkv, MB, want):
     monkeypatch.delenv("FORGE_DECODE_KERNEL", raising=False)
@@ -271,7 +271,7 @@ def test_decode_plan_policy(lib, monkeypatch, B, Hkv, MB, want):
 def test_decode_plan_explicit_split_and_override(lib, monkeypatch):
     monkeypatch.delenv("FORGE_DECODE_KERNEL", raising=False)
     assert binding.forge_paged_gqa_decode_plan(32, 8, 498, 512, num_sms=152) == (512, "online")
-    assert binding.forge_paged_gqa_decode_plan(32, 8, 498, 496, num_sms=152) == (496, "two_pass")
+    assert binding.forge_paged_gqa_decode_plan(32, 8, 498, 496, num_sms=152) == (496, "online")
     monkeypatch.setenv("FORGE_DECODE_KERNEL", "two_pass")   # automatic two-pass splits stop at 512
     assert binding.forge_paged_gqa_decode_plan(32, 8, 498, 0, num_sms=152) == (512, "two_pass")
     assert binding.forge_paged_gqa_decode_plan(32, 8, 498, 1024, num_sms=152) == (1024, "two_pass")
