@@ -83,6 +83,20 @@ struct TcLayout {
 
 // Q [tile][box][128 rows][128 B] | K ring [stage][box][128 tok][128 B] |
 // V ring (same) | mbarriers, TMEM slot.  Offsets from a 1024-byte-aligned base.
+// Whether the phase of `bar` with this parity has completed, without waiting
+// (acquire semantics when it has).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __host__ __device__ constexpr int q_tile_bytes(int D) { return (D / 64) * kTcRows * 128; }
 __host__ __device__ constexpr int kv_stage_bytes(int D) { return (D / 64) * kTcKv * 128; }
 __host__ __device__ constexpr TcLayout tc_layout(int D) {
@@ -410,14 +424,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // P over S_t: K step kk (16 tokens) is in chunk kk / 2 (32 columns):
         // high parts at 32 (kk / 2) + 8 (kk % 2), low parts 16 columns on.
         // The first half of the K steps runs once the softmax has written the
-        // first 64 tokens' weights, while it computes the rest.
+        // first 64 tokens' weights, while it computes the rest; when all of
+        // P_t is already written, all of them go out at once.  V_j has landed
+        // by then: tile 0's softmax warps wait for it before their first
+        // arrival of the stage.
         const uint32_t pcol = tmem + kColS + kTcRows * t, dout = tmem + kColO + kTcRows * t;
+        const bool whole = __all_sync(kFullMask, mbar_test(bars + kPFull + t, j & 1));
+        if (whole) tc::fence_after_sync();
         for (int half = 0; ok && half < 2; ++half) {
-          ok = mbar_wait(bars + (half == 0 ? kPHalf : kPFull) + t, j & 1, p.err);
-          if (ok && t == 0 && half == 0) ok = mbar_wait(bars + kVFull + sv, (j / kTcVStages) & 1, p.err);
-          ok = __all_sync(kFullMask, ok);
-          if (!ok) break;
-          tc::fence_after_sync();
+          if (!whole) {
+            ok = mbar_wait(bars + (half == 0 ? kPHalf : kPFull) + t, j & 1, p.err);
+            ok = __all_sync(kFullMask, ok);
+            if (!ok) break;
+            tc::fence_after_sync();
+          }
 #pragma unroll
           for (int k2 = 0; k2 < PSTEPS / 2; ++k2) {
             const int kk = half * (PSTEPS / 2) + k2;
@@ -568,6 +588,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
         }
         if (h2 == 0) {  // the first 64 tokens' weights: their half of P_t V may start
+          // V_j landed before the stage's first arrival (the MMA warp relies on it)
+          if (t == 0) mbar_wait(bars + kVFull + j % kTcVStages, (j / kTcVStages) & 1, p.err);
           tc::wait_st();
           tc::fence_before_sync();
           __syncwarp();
