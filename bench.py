@@ -76,10 +76,12 @@ DECODE_KERNELS = {"online": "paged_gqa_decode_online_kernel", "two_pass": "paged
 PROFILE_FILES = {"online": "decode_online_qwen3_4b.md", "two_pass": "decode_split_qwen3_4b.md"}
 
 
-def _traffic_from_profile(src_hash: str, kernel: str):
-    """DRAM bytes per Qwen3-4B decode launch of `kernel` from its committed ncu
-    summary, if that was taken on the current decode source; else None."""
-    p = os.path.join(ROOT, "profiles", PROFILE_FILES[kernel])
+def _traffic_from_profile(src_hash: str, kernel: str, profile: str | None = None,
+                          key: str = "dram_bytes_per_decode_call"):
+    """DRAM bytes per launch of `kernel` (the Qwen3-4B decode launch, or with
+    `profile` and `key` another kernel's) from its committed ncu summary, if
+    that was taken on the current source; else None."""
+    p = os.path.join(ROOT, "profiles", profile or PROFILE_FILES[kernel])
     if not os.path.exists(p):
         return None
     vals = {}
@@ -90,17 +92,25 @@ def _traffic_from_profile(src_hash: str, kernel: str):
     if vals.get("source_sha256") != src_hash:
         return None
     try:
-        return int(vals["dram_bytes_per_decode_call"])
+        return int(vals[key])
     except (KeyError, ValueError):
         return None
 
 
-def _decode_source_hash():
+def _source_hash(files):
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh", "abi.cu"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_gqa_06_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def _decode_source_hash():
+    return _source_hash(("decode.cu", "common.cuh", "abi.cu"))
+
+
+def _prefill_source_hash():
+    return _source_hash(("prefill_tc.cu", "tcgen05.cuh", "common.cuh", "abi.cu"))
 
 
 class ClockSampler:
@@ -996,6 +1006,11 @@ def run_prefill(args, name):
     else:
         peak, peak_src = 1900.0, "fallback (1.9 PFLOP/s bf16 burst), of fallback"
     tflops_kernel = flops / (ms_kernel * 1e-3) / 1e12
+    # DRAM bytes per launch from the committed ncu summary of the tcgen05 kernel
+    # on this workload, if it was taken on the current sources
+    traffic = (_traffic_from_profile(_prefill_source_hash(), "", "prefill_qwen3_4b.md",
+                                     "dram_bytes_per_prefill_call")
+               if name == "prefill_4b" and os.environ.get("FORGE_PREFILL_KERNEL") != "mma" else None)
     tflops_step = flops / (ms_step * 1e-3) / 1e12
     return {
         "metric": "paged prefill: attention TFLOP/s (causal pairs only) and us per call",
@@ -1012,7 +1027,7 @@ def run_prefill(args, name):
                                 if os.environ.get("FORGE_PREFILL_KERNEL") == "mma" else
                                 "paged_prefill_tc_kernel (tcgen05.mma, accumulators in TMEM, P from TMEM)"),
                      "achieved": round(tflops_kernel, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tflops_kernel / peak, 4), "traffic": None,
+                     "frac": round(tflops_kernel / peak, 4), "traffic": traffic,
                      "prefill_us": round(ms_kernel * 1e3, 2), "peak_source": peak_src},
         "gpu_launches": 2 * reps * copies,
         "clocks": clocks,

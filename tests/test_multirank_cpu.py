@@ -136,3 +136,22 @@ def test_reference_arm_has_the_gpu_arms_config():
     assert cfg["bytes_per_step"] == wl.bytes_decode(2) and cfg["layers"] == 1
     small = bench._config_dict(W.make_workload("qwen3_0_6b"), Args(), 2)
     assert "copies of the KV pools rotated" in small["l2"]
+
+
+def test_profile_traffic_is_read_only_for_matching_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only when the
+    summary names the hash of the sources the bench is running."""
+    sys.path.insert(0, ROOT)
+    import bench
+    (tmp_path / "profiles").mkdir()
+    prof = tmp_path / "profiles" / "k.md"
+    prof.write_text("# k\n\n- source_sha256: `abc123`\n- dram_bytes_per_prefill_call: `1234`\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._traffic_from_profile("abc123", "", "k.md", "dram_bytes_per_prefill_call") == 1234
+    assert bench._traffic_from_profile("other", "", "k.md", "dram_bytes_per_prefill_call") is None
+    assert bench._traffic_from_profile("abc123", "", "k.md", "dram_bytes_per_decode_call") is None
+    assert bench._traffic_from_profile("abc123", "", "missing.md") is None
+    # the hashes cover the kernel sources and differ between the two paths
+    monkeypatch.setattr(bench, "ROOT", ROOT)
+    assert bench._decode_source_hash() != bench._prefill_source_hash()
+    assert len(bench._decode_source_hash()) == 16
