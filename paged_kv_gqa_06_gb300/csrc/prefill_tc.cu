@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the whole warp (one path per warp, not one per row)
       const bool masked = __any_sync(kFullMask, t0 + kTcKv - 1 > lim);
       // pass 1: the row's maximum over the stage (four loads, one wait)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
       {
         uint32_t v[kTcKv];
 #pragma unroll
@@ -492,10 +492,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::ld_32x32b_x32(trow + scol + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * h));
         tc::wait_ld();
         if (!masked) {
+          // four independent chains of three-input maxima
 #pragma unroll
-          for (int c = 0; c < kTcKv; c += 4) {
+          for (int c = 0; c < kTcKv; c += 8) {
             mx0 = fmax3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             mx1 = fmax3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
           }
         } else {
 #pragma unroll
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      const float mx = fmaxf(mx0, mx1);
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       // every row sees token 0 in the first stage, so m_new is finite
       const float m_new = fmaxf(m_used, mx * scale);
       const bool need = m_new > m_used + kRescaleSlack;
@@ -552,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // go over its own 32 columns, which it has just read: bf16 high parts in
       // [32h, 32h + 16), low parts in [32h + 16, 32h + 32), two per column.
       const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m_used, -m_used);
-      float2 l2 = make_float2(0.f, 0.f);
+      float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two independent sum chains
 #pragma unroll 1
       for (int h2 = 0; h2 < kTcKv / 64; ++h2) {  // two chunks of 32 per TMEM wait
         uint32_t v[64];
@@ -569,7 +572,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float2 y = ffma2(make_float2(__uint_as_float(v[32 * hh + 2 * e]), __uint_as_float(v[32 * hh + 2 * e + 1])),
                                      sc2, nm2);
               const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-              l2 = fadd2(l2, w);
+              l2[e & 1] = fadd2(l2[e & 1], w);
               split_bf16x2(w.x, w.y, hi[e], lo[e]);
             }
           } else {
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float x1 = tb + 2 * e + 1 <= lim ? __uint_as_float(v[32 * hh + 2 * e + 1]) : -INFINITY;
               const float2 y = ffma2(make_float2(x0, x1), sc2, nm2);
               const float2 w = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-              l2 = fadd2(l2, w);
+              l2[e & 1] = fadd2(l2[e & 1], w);
               split_bf16x2(w.x, w.y, hi[e], lo[e]);
             }
           }
@@ -596,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) mbar_arrive(bars + kPHalf + t);
         }
       }
-      l += l2.x + l2.y;
+      l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
       tc::wait_st();
       tc::fence_before_sync();  // P stores in TMEM before the arrival
       __syncwarp();
