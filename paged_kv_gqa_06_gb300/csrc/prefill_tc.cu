@@ -556,12 +556,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // [32h, 32h + 16), low parts in [32h + 16, 32h + 32), two per column.
       const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m_used, -m_used);
       float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two independent sum chains
+      uint32_t v[64];
+      tc::ld_32x32b_x32(trow + scol, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tc::ld_32x32b_x32(trow + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tc::wait_ld();
 #pragma unroll 1
-      for (int h2 = 0; h2 < kTcKv / 64; ++h2) {  // two chunks of 32 per TMEM wait
-        uint32_t v[64];
-        tc::ld_32x32b_x32(trow + scol + 64 * h2, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tc::ld_32x32b_x32(trow + scol + 64 * h2 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tc::wait_ld();
+      for (int h2 = 0; h2 < kTcKv / 64; ++h2) {  // two chunks of 32 per TMEM read
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int h = 2 * h2 + hh;
@@ -591,12 +591,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::st_32x32b_x16(trow + scol + 32 * h + 16, lo);
         }
         if (h2 == 0) {  // the first 64 tokens' weights: their half of P_t V may start
+          // the next 64 scores are read while these weights land in TMEM
+          tc::ld_32x32b_x32(trow + scol + 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tc::ld_32x32b_x32(trow + scol + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           // V_j landed before the stage's first arrival (the MMA warp relies on it)
           if (t == 0) mbar_wait(bars + kVFull + j % kTcVStages, (j / kTcVStages) & 1, p.err);
           tc::wait_st();
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bars + kPHalf + t);
+          tc::wait_ld();
         }
       }
       l += (l2[0].x + l2[1].x) + (l2[0].y + l2[1].y);
