@@ -40,8 +40,9 @@
 //     the row's maximum grows by more than 8 in log2 units, so the weights
 //     stay <= 2^8 and O is rescaled rarely (O_t is idle then: the previous
 //     P_t V has completed before S_t was written).  The row is read twice
-//     from TMEM, for its maximum and then 32 tokens at a time for the
-//     weights, which keeps the registers of 320 threads within the SM.  The
+//     from TMEM, for its maximum and then 64 tokens at a time for the
+//     weights (the second 64 while the first 64's weights are stored), which
+//     keeps the registers of 320 threads within the SM.  The
 //     weights P = 2^(scale s - m) go over the 32 columns of S they came from,
 //     as bf16 high parts (16 columns, two weights per column) and low parts
 //     (the next 16), so P V keeps ~16 bits of each weight: a weight rounded
