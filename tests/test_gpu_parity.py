@@ -295,8 +295,10 @@ def test_scratch_cannot_grow_during_capture():
     s = torch.cuda.Stream()
     out = out_tensor(wl, "f32")
     g = torch.cuda.CUDAGraph()
+    # thread-local capture: only this thread's calls (the library's among them)
+    # may invalidate it, not another thread of the test process
     with pytest.raises(binding.ForgeError) as info:
-        with torch.cuda.graph(g, stream=s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
             binding.forge_paged_gqa_decode(d.q, d.k_cache, d.v_cache, d.tables, d.lens, wl.scale, out, stream=s)
     assert info.value.status == -7
     with torch.cuda.stream(s):
@@ -304,7 +306,7 @@ def test_scratch_cannot_grow_during_capture():
     s.synchronize()
     g2 = torch.cuda.CUDAGraph()
     out2 = out_tensor(wl, "f32")
-    with torch.cuda.graph(g2, stream=s):
+    with torch.cuda.graph(g2, stream=s, capture_error_mode="thread_local"):
         binding.forge_paged_gqa_decode(d.q, d.k_cache, d.v_cache, d.tables, d.lens, wl.scale, out2, stream=s)
     g2.replay()
     torch.cuda.synchronize()
