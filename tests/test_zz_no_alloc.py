@@ -5,11 +5,12 @@ serving loop that gave the rest to its KV-block pool), or code running under
 a memory manager of its own that forbids allocations it did not make -- call
 this entry point instead of forge_paged_gqa_decode, which may allocate its
 split scratch on first use.
-This test calls it through the C ABI twice in a row (the static scratch keeps
-the first call's contents) and checks both results against the regular entry
-point's within the parity tolerance.  It lives in a file of its own that
-pytest collects last, and it builds its own inputs so it also passes alone in
-a fresh process.
+These tests call it through the C ABI twice in a row (the static scratch keeps
+the first call's contents) and check both results against the regular entry
+point's within the parity tolerance, with shapes alternating over the one
+scratch, and with the device's free memory unchanged across calls.  They live
+in a file of their own that pytest collects last, and build their own inputs
+so they also pass alone in a fresh process.
 """
 import ctypes
 
@@ -102,3 +103,26 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = lib.forge_paged_gqa_decode_noalloc(*(ctypes.byref(x) for x in descs[:5]), ctypes.c_float(0.1),
                                             ctypes.byref(descs[5]), torch.cuda.current_stream().cuda_stream)
     assert rc == -7   # FORGE_ERR_WORKSPACE: needs more than the static scratch holds
+
+
+def test_noalloc_calls_leave_device_free_memory_unchanged():
+    """After one warm-up call (which may load the kernel's code), further
+    calls allocate nothing: the device's free memory is the same after them.
+    The output tensors are made before the measurement, and nothing else in
+    this process allocates in between."""
+    lib = binding.load_library()
+    wl = W.make_workload("skewed")
+    t = wl.layer(0)
+    d = DeviceLayer(wl, t)
+    d.append()
+    outs = [out_tensor(wl) for _ in range(4)]
+    assert _call_noalloc(lib, d, outs[0]) == 0
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for out in outs[1:]:
+        assert _call_noalloc(lib, d, out) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert binding.forge_paged_get_device_error() == 0
+    for out in outs[1:]:
+        assert torch.equal(out, outs[0])
