@@ -622,8 +622,10 @@ def run_native(args, wl, out_bytes):
     # Every step uploads its inputs from pinned host memory (one packed
     # buffer: q, k_new, v_new, slots, tables, lens) and reads its output back
     # to pinned host memory.  Uploads and read-backs run on their own streams
-    # with two device buffer sets, so step i+1's upload and step i-1's
-    # read-back overlap step i's compute, as a serving loop would run them.
+    # with NSETS device buffer sets, so later steps' uploads and earlier steps'
+    # read-backs overlap step i's compute, as a serving loop would run them;
+    # with four sets every event a step waits for has long completed.
+    NSETS = 4
     host, d, out = rig.host, rig.d, rig.d["out"]
     out_dt = rig.out_dt
     fields = ("q", "k_new", "v_new", "slots", "tables", "lens")
@@ -635,31 +637,31 @@ def run_native(args, wl, out_bytes):
     host_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
     for k in fields:
         host_pack[offs[k]:offs[k] + nbytes[k]].copy_(host[k].contiguous().view(-1).view(torch.uint8))
-    dev_pack = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
-    out_e = [torch.empty_like(out) for _ in range(2)]
-    host_out_e = [torch.empty(out.shape, dtype=out_dt).pin_memory() for _ in range(2)]
+    dev_pack = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(NSETS)]
+    out_e = [torch.empty_like(out) for _ in range(NSETS)]
+    host_out_e = [torch.empty(out.shape, dtype=out_dt).pin_memory() for _ in range(NSETS)]
     views = []
-    for sb in range(2):
+    for sb in range(NSETS):
         v = {k: dev_pack[sb][offs[k]:offs[k] + nbytes[k]].view(host[k].dtype).view(host[k].shape) for k in fields}
         v["out"] = out_e[sb]
         views.append(v)
     h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_h2d = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+    ev_h2d = [torch.cuda.Event() for _ in range(NSETS)]
+    ev_comp = [torch.cuda.Event() for _ in range(NSETS)]
+    ev_d2h = [torch.cuda.Event() for _ in range(NSETS)]
     saved = dict(d)
 
     def e2e_run(n, t0=None, t1=None):
         if t0 is not None:
             t0.record(h2d_s)
-        for sb in range(min(2, n)):
+        for sb in range(min(NSETS, n)):
             with torch.cuda.stream(h2d_s):
                 dev_pack[sb].copy_(host_pack, non_blocking=True)
             ev_h2d[sb].record(h2d_s)
         for i in range(n):
-            sb = i & 1
+            sb = i % NSETS
             stream.wait_event(ev_h2d[sb])
-            if i >= 2:
+            if i >= NSETS:
                 stream.wait_event(ev_d2h[sb])      # this buffer set's previous output is read back
             d.update(views[sb])
             with torch.cuda.stream(stream):
@@ -669,7 +671,7 @@ def run_native(args, wl, out_bytes):
             with torch.cuda.stream(d2h_s):
                 host_out_e[sb].copy_(out_e[sb], non_blocking=True)
             ev_d2h[sb].record(d2h_s)
-            if i + 2 < n:
+            if i + NSETS < n:
                 h2d_s.wait_event(ev_comp[sb])      # this buffer set's inputs are consumed
                 with torch.cuda.stream(h2d_s):
                     dev_pack[sb].copy_(host_pack, non_blocking=True)
@@ -686,7 +688,7 @@ def run_native(args, wl, out_bytes):
     torch.cuda.synchronize(dev)
     e2e_ms = e2e_start.elapsed_time(e2e_end)
     d.update(saved)
-    host_out = host_out_e[(args.steps - 1) & 1]
+    host_out = host_out_e[(args.steps - 1) % NSETS]
     assert binding.forge_paged_get_device_error(stream) == 0
     assert torch.isfinite(host_out.float()).all()
 
@@ -736,7 +738,7 @@ def run_native(args, wl, out_bytes):
                 "ms_per_step": round(e2e_ms / args.steps, 5),
                 "how": "every step: its packed inputs copied from pinned host memory, the step through the "
                        "public binding (eager calls), its output copied back to pinned host memory; copies on "
-                       "their own streams, two buffer sets, overlapping the neighbouring steps' compute"},
+                       f"their own streams, {NSETS} buffer sets, overlapping the neighbouring steps' compute"},
         "gpu_launches": launches_per_step * args.steps,
         "path": PATH_NAMES[args.path],
         "other_paths": {k: {"path": PATH_NAMES[k], "ms_per_step": round(v / args.steps, 5),
