@@ -74,6 +74,9 @@ def _peaks():
 
 DECODE_KERNELS = {"online": "paged_gqa_decode_online_kernel", "two_pass": "paged_gqa_decode_split_kernel"}
 PROFILE_FILES = {"online": "decode_online_qwen3_4b.md", "two_pass": "decode_split_qwen3_4b.md"}
+# The single-pass kernel's ncu summary on the two latency-bound workloads, one traffic key each.
+LATENCY_PROFILE = "decode_online_latency_workloads.md"
+LATENCY_WORKLOADS = ("qwen3_0_6b", "skewed")
 
 
 def _traffic_from_profile(src_hash: str, kernel: str, profile: str | None = None,
@@ -107,6 +110,17 @@ def _source_hash(files):
 
 def _decode_source_hash():
     return _source_hash(("decode.cu", "common.cuh", "abi.cu"))
+
+
+def _decode_traffic(workload: str, kern: str):
+    """DRAM bytes per decode launch on `workload` from the committed ncu
+    summary that covers it, or None where none does."""
+    if workload == "qwen3_4b":
+        return _traffic_from_profile(_decode_source_hash(), kern)
+    if workload in LATENCY_WORKLOADS and kern == "online":
+        return _traffic_from_profile(_decode_source_hash(), kern, LATENCY_PROFILE,
+                                     f"dram_bytes_per_decode_call_{workload}")
+    return None
 
 
 def _prefill_source_hash():
@@ -708,7 +722,7 @@ def run_native(args, wl, out_bytes):
     dec_avg_ms = statistics.fmean(decode_ms)
     achieved = bytes_layer / (dec_avg_ms * 1e-3) / 1e9
     split_tokens, kern = binding.forge_paged_gqa_decode_plan(wl.B, wl.Hkv, wl.MB)
-    traffic = _traffic_from_profile(_decode_source_hash(), kern) if wl.spec.name == "qwen3_4b" else None
+    traffic = _decode_traffic(wl.spec.name, kern)
     h2d = total  # the packed input buffer, as copied each step
     d2h = host_out.numel() * host_out.element_size()
     tol = TOL[wl.spec.out_dtype]

@@ -151,6 +151,16 @@ def test_profile_traffic_is_read_only_for_matching_sources(tmp_path, monkeypatch
     assert bench._traffic_from_profile("other", "", "k.md", "dram_bytes_per_prefill_call") is None
     assert bench._traffic_from_profile("abc123", "", "k.md", "dram_bytes_per_decode_call") is None
     assert bench._traffic_from_profile("abc123", "", "missing.md") is None
+    # each latency-bound workload reads its own key from the shared summary
+    monkeypatch.setattr(bench, "_decode_source_hash", lambda: "abc123")
+    (tmp_path / "profiles" / bench.LATENCY_PROFILE).write_text(
+        "- source_sha256: `abc123`\n- dram_bytes_per_decode_call_qwen3_0_6b: `11`\n"
+        "- dram_bytes_per_decode_call_skewed: `22`\n")
+    assert bench._decode_traffic("qwen3_0_6b", "online") == 11
+    assert bench._decode_traffic("skewed", "online") == 22
+    assert bench._decode_traffic("skewed", "two_pass") is None
+    assert bench._decode_traffic("cb36", "online") is None
+    monkeypatch.undo()
     # the hashes cover the kernel sources and differ between the two paths
     monkeypatch.setattr(bench, "ROOT", ROOT)
     assert bench._decode_source_hash() != bench._prefill_source_hash()
