@@ -195,6 +195,42 @@ def test_cuda_graph_replay_matches_eager():
     assert max_abs_err(out, oracle_decode(wl, t, kc_ref, vc_ref)) <= TOL["bf16"]
 
 
+def test_lengths_written_by_the_previous_kernel():
+    """Each decode's lengths are written by the kernel just before it in the
+    stream: an append whose destination row is the length array (an int32
+    view of a scratch bf16 cache).  That append lets its dependent launch
+    start early, so a decode CTA may read the previous lengths before
+    griddepcontrol.wait and predict the wrong first blocks.  Every call must
+    still decode the lengths that the append wrote."""
+    wl, t, (kc_ref, vc_ref) = _config("qwen3_0_6b")
+    d = DeviceLayer(wl, t)
+    d.append()
+    lens_a = wl.context_lens.astype(np.int32)
+    lens_b = np.maximum(lens_a - 37, 1).astype(np.int32)  # other block counts, so other split boundaries
+    scratch_k = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device=DEV)
+    scratch_v = torch.zeros_like(scratch_k)
+    lens_dev = scratch_k.view(torch.int32).view(-1)[: wl.B]  # row 0 of block 0, head 0
+    zero_slot = torch.zeros(1, dtype=torch.int64, device=DEV)
+
+    def row_of(lens):
+        r = np.zeros(32, dtype=np.int32)
+        r[: wl.B] = lens
+        return torch.from_numpy(r.view(np.int16).copy()).view(torch.bfloat16).reshape(1, 1, 64).to(DEV)
+
+    rows = {"a": row_of(lens_a), "b": row_of(lens_b)}
+    order = ["a", "b"] * 8
+    outs = [out_tensor(wl, "bf16") for _ in order]
+    for key, out in zip(order, outs):  # back to back, no host sync in between
+        binding.forge_paged_kv_append(rows[key], rows[key], zero_slot, scratch_k, scratch_v)
+        binding.forge_paged_gqa_decode(d.q, d.k_cache, d.v_cache, d.tables, lens_dev, wl.scale, out)
+    torch.cuda.synchronize()
+    assert_device_clean()
+    refs = {"a": oracle_decode(wl, t, kc_ref, vc_ref, lens=lens_a),
+            "b": oracle_decode(wl, t, kc_ref, vc_ref, lens=lens_b)}
+    for key, out in zip(order, outs):
+        assert max_abs_err(out, refs[key]) <= TOL["bf16"], key
+
+
 def test_device_side_precondition_checks_report_errors():
     wl, t, _ = _config("tiny")
     d = DeviceLayer(wl, t)
