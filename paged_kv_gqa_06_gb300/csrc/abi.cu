@@ -226,13 +226,14 @@ int decode_kernel_forced() {
 // parallelism (measured: Qwen3-0.6B-shaped batch of 8, 12.8 us at 128-token
 // splits against 16.0 us at 64).
 //
-// Kernel: splits of 512 tokens or more run the single-pass online-softmax
-// kernel, whose shared memory is all K/V ring (more bytes in flight per SM);
-// shorter ones the two-pass kernel, whose small logits buffer leaves room for
-// 8 CTAs per SM.  Measured on GB300, decode of one layer: Qwen3-4B-shaped
+// Kernel: the single-pass online-softmax kernel at every split length (its
+// shared memory is all K/V ring, so more bytes are in flight per SM).  On
+// short splits its ring is 2 stages deep, which lets a fifth CTA onto each SM
+// (nstage_for).  Measured on GB300, decode of one layer: Qwen3-4B-shaped
 // batch of 32, 93.6 us single-pass at 1024 tokens against 97.9 us two-pass at
-// 512; Qwen3-0.6B-shaped batch of 8, 11.7 us two-pass at 128 tokens against
-// 14.9 us single-pass.  FORGE_DECODE_KERNEL overrides the kernel.
+// 512; Qwen3-0.6B-shaped batch of 8, 10.97 us single-pass at 128 tokens with
+// 2 stages against 11.72 us two-pass.  FORGE_DECODE_KERNEL=two_pass selects
+// the two-pass kernel.
 int split_blocks_for(int split_tokens, int B, int Hkv, int MB, int num_sms, int* online) {
   int bps = kMaxSplitTokens / kBlockSize;
   if (split_tokens > 0) {
